@@ -1,0 +1,48 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
+
+Recipe: Q, K, V and the upstream gradient dO are drawn, in that order, as N(0, 1)
+float32 from one ``torch.Generator`` seeded with ``seed``, shape [B, L, H, D], and
+rounded to bfloat16 (round to nearest even).  The oracle receives the same rounded
+values widened to float64.  This module holds no attention arithmetic.
+"""
+
+import torch
+
+# The five workloads of this library's test and benchmark plan.
+WORKLOADS = {
+    "tiny":  dict(batch=1, heads=2, head_dim=64, seq_len=512, P=4, block=128,
+                  causal=False, layouts=("contiguous",), backward=False),
+    "8k":    dict(batch=1, heads=8, head_dim=128, seq_len=8192, P=8, block=128,
+                  causal=True, layouts=("contiguous", "striped"), backward=False),
+    "32k":   dict(batch=1, heads=32, head_dim=128, seq_len=32768, P=8, block=128,
+                  causal=True, layouts=("striped",), backward=True),
+    "262k":  dict(batch=1, heads=32, head_dim=128, seq_len=262144, P=16, block=256,
+                  causal=True, layouts=("striped",), backward=True),
+    "1m":    dict(batch=1, heads=8, head_dim=128, seq_len=1048576, P=32, block=256,
+                  causal=True, layouts=("striped", "contiguous"), backward=True),
+}
+
+SEEDS = {"tiny": 1000, "8k": 1001, "32k": 1002, "262k": 1003, "1m": 1004}
+
+
+def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=True):
+    """Return (q, k, v[, dout]) bfloat16 tensors [B, L, H, D] on ``device``.
+
+    The generator lives on ``device``; CPU and CUDA streams of numbers differ, so
+    a test that compares against the oracle generates on the CPU (or copies device
+    tensors to the host) and hands the same tensors to both sides.
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    shape = (batch, seq_len, heads, head_dim)
+    names = ("q", "k", "v", "dout") if with_dout else ("q", "k", "v")
+    out = []
+    for _ in names:
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        out.append(x.to(torch.bfloat16))
+    return tuple(out)
+
+
+def to_f64(*tensors):
+    """bfloat16 torch tensors -> float64 NumPy arrays (exact widening)."""
+    return tuple(t.detach().to("cpu", torch.float64).numpy() for t in tensors)

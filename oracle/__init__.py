@@ -1,0 +1,44 @@
+"""CPU fp64 oracle for exact blockwise ring attention (contiguous and striped).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import or run anything in this package.  The
+product path (the CUDA library and its Python binding) never imports it, and this
+package imports nothing from the product path.
+
+Sources (four web pages on Ring Attention and Striped Attention):
+
+* "Ring Attention 論文分析" (labhub): the BPT blockwise online softmax
+  (section "ブロック単位の分割戦略"), the ring forward (section "リングトポロジーと
+  KV の循環"), causal block skipping (section "Causal Masking の処理"), the ring
+  order (section "リング通信パターン") and the backward formulas (section
+  "逆伝播での KV 再循環").
+* "Ring Attention: Sequence Parallelism for Long Context" (vanos001): the ring
+  diagram, the striped assignment (section "The Causal-Mask Problem: Striped
+  Attention") and the worked demo of per-device work (section "Worked Demo").
+* "Sequence parallelism and ring attention" (aiunderstanding) and the Striped
+  Attention summary (aibr.jp, section 3, permutation equivariance).
+
+Modules:
+    attention -- exact attention forward/backward by its definition (row-blocked
+                 full-row softmax, no online merge, no ring) and a brute-force
+                 pure-Python version for tiny inputs.
+    ring      -- an fp64 emulator of the ring schedule with online softmax and the
+                 partial merge, used only to test invariants ("ring == full").
+    work      -- shard assignment, ring order and the per-shard work model.
+
+Parity status: every function here is pinned by tests in ``tests/test_oracle_*.py``
+against things other than itself (a library softmax attention, closed forms,
+finite differences, the pages' printed demo output).  None is "parity unpinned".
+"""
+
+from .attention import (attention_fwd, attention_bwd, attention_rows_fwd,
+                        brute_force_fwd, default_scale)
+from .ring import ring_fwd, ring_partials, merge_partials
+from .work import (shard_of, local_of, shard_tokens, ring_order, shard_work,
+                   tile_class)
+
+__all__ = [
+    "attention_fwd", "attention_bwd", "attention_rows_fwd", "brute_force_fwd",
+    "default_scale", "ring_fwd", "ring_partials", "merge_partials", "shard_of",
+    "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class",
+]
