@@ -1,0 +1,13 @@
+"""Exact blockwise ring attention (contiguous and striped) for NVIDIA GB300 (sm_103a).
+
+The computation lives in libra.so (C ABI: include/ra.h), built from csrc/ by
+``exact_blockwise_ring_gb300.build.build()``; this package only marshals arguments.
+"""
+
+from .api import (LAYOUTS, Params, RaError, RingAttention, Workspace, bwd_workspace_bytes,
+                  fwd_workspace_bytes, header_symbols, lib, make_params, ra_bwd, ra_fwd,
+                  ra_merge, ra_selftest_timeout, ra_shard_work_model, ring_attention)
+
+__all__ = ["LAYOUTS", "Params", "RaError", "RingAttention", "Workspace", "bwd_workspace_bytes",
+           "fwd_workspace_bytes", "header_symbols", "lib", "make_params", "ra_bwd", "ra_fwd",
+           "ra_merge", "ra_selftest_timeout", "ra_shard_work_model", "ring_attention"]

@@ -1,0 +1,241 @@
+"""ctypes binding of libra.so (the C ABI in include/ra.h).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the library has
+not been built, every call raises; there is no fallback path.
+"""
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libra.so")
+HEADER_PATH = os.path.join(_HERE, "..", "include", "ra.h")
+
+LAYOUTS = {"contiguous": 0, "striped": 1}
+STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_WORKSPACE",
+          4: "RA_ERR_CUDA", 5: "RA_ERR_DEVICE_TIMEOUT"}
+RA_BF16, RA_FP32 = 0, 1
+
+
+class Params(ctypes.Structure):
+    """Mirror of ra_params_t."""
+    _fields_ = [("batch", ctypes.c_int), ("seq_len", ctypes.c_int64), ("heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("block", ctypes.c_int), ("P", ctypes.c_int),
+                ("layout", ctypes.c_int), ("causal", ctypes.c_int),
+                ("softmax_scale", ctypes.c_float), ("n_split", ctypes.c_int)]
+
+
+class RaError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        super().__init__("%s: %s" % (STATUS.get(status, status), message))
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "ra_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Params)]),
+    "ra_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Params)]),
+    "ra_fwd": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, ctypes.c_int, _P, _P, _P,
+                              ctypes.c_size_t, _P]),
+    "ra_bwd": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, ctypes.c_int, _P, _P, _P,
+                              _P, _P, _P, ctypes.c_size_t, _P]),
+    "ra_merge": (ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                ctypes.c_int, _P, ctypes.c_int, _P, _P]),
+    "ra_shard_work_model": (ctypes.c_int, [ctypes.POINTER(Params),
+                                           ctypes.POINTER(ctypes.c_ulonglong)]),
+    "ra_check_error": (ctypes.c_int, [_P, _P]),
+    "ra_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint, _P]),
+    "ra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ra_last_error_message": (ctypes.c_char_p, []),
+}
+
+
+def lib():
+    """Load libra.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libra.so is not built: run exact_blockwise_ring_gb300.build."
+                                   "build() (needs nvcc for sm_103a)")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(h, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = h
+    return _lib
+
+
+def header_symbols():
+    """Names of the functions declared in include/ra.h."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"\b(ra_[a-z_]+)\s*\(", text)))
+
+
+def _check(status):
+    if status != 0:
+        msg = lib().ra_last_error_message().decode(errors="replace")
+        raise RaError(status, msg)
+
+
+def make_params(batch, seq_len, heads, head_dim, P, block, layout="contiguous", causal=True,
+                softmax_scale=0.0, n_split=0):
+    if isinstance(layout, str):
+        layout = LAYOUTS[layout]
+    return Params(int(batch), int(seq_len), int(heads), int(head_dim), int(block), int(P),
+                  int(layout), int(bool(causal)) if isinstance(causal, bool) else int(causal),
+                  float(softmax_scale), int(n_split))
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check_qkv(*ts):
+    shape = ts[0].shape
+    for t in ts:
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != shape:
+            raise ValueError("q, k, v (and dout) must be contiguous CUDA bf16 tensors of one "
+                             "[B, L, H, D] shape")
+    if len(shape) != 4:
+        raise ValueError("expected [B, L, H, D]")
+    return shape
+
+
+class Workspace:
+    """A zero-initialised device buffer reused across calls (grown on demand)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = torch.zeros(256, dtype=torch.uint8, device=self.device)
+
+    def get(self, nbytes):
+        if self.buf.numel() < nbytes:
+            self.buf = torch.zeros(int(nbytes), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+    def check(self, stream=None):
+        """Sync the stream and raise RaError if a kernel gave up a wait."""
+        _check(lib().ra_check_error(_ptr(self.buf), _stream(stream)))
+
+
+_default_ws = {}
+
+
+def default_workspace(device):
+    key = torch.device(device).index or 0
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(torch.device("cuda", key))
+    return _default_ws[key]
+
+
+def fwd_workspace_bytes(params):
+    return lib().ra_fwd_workspace_bytes(ctypes.byref(params))
+
+
+def bwd_workspace_bytes(params):
+    return lib().ra_bwd_workspace_bytes(ctypes.byref(params))
+
+
+def ra_fwd(q, k, v, P, block, layout="contiguous", causal=True, softmax_scale=0.0,
+           out_dtype=torch.bfloat16, n_split=0, shard_work=False, workspace=None, stream=None,
+           out=None, lse=None):
+    """Forward pass through ra_fwd.  Returns (out, lse) or (out, lse, shard_work[3, P])."""
+    B, L, H, D = _check_qkv(q, k, v)
+    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, n_split)
+    if out is None:
+        out = torch.empty((B, L, H, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    odt = RA_FP32 if out.dtype == torch.float32 else RA_BF16
+    sw = torch.empty(3 * P, dtype=torch.int64, device=q.device) if shard_work else None
+    ws = workspace or default_workspace(q.device)
+    need = fwd_workspace_bytes(prm)
+    buf = ws.get(max(need, 256))
+    _check(lib().ra_fwd(ctypes.byref(prm), _ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse),
+                        _ptr(sw), _ptr(buf), buf.numel(), _stream(stream)))
+    if shard_work:
+        return out, lse, sw.view(3, P)
+    return out, lse
+
+
+def ra_bwd(q, k, v, out, lse, dout, P, block, layout="contiguous", causal=True,
+           softmax_scale=0.0, workspace=None, stream=None, dq=None, dk=None, dv=None):
+    """Backward pass through ra_bwd.  Returns (dq, dk, dv) bf16."""
+    B, L, H, D = _check_qkv(q, k, v, dout)
+    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, 0)
+    odt = RA_FP32 if out.dtype == torch.float32 else RA_BF16
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace or default_workspace(q.device)
+    need = bwd_workspace_bytes(prm)
+    buf = ws.get(max(need, 256))
+    _check(lib().ra_bwd(ctypes.byref(prm), _ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse),
+                        _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(buf), buf.numel(),
+                        _stream(stream)))
+    return dq, dk, dv
+
+
+def ra_merge(o_parts, lse_parts, out_dtype=torch.bfloat16, stream=None):
+    """Merge partials o_parts [n, B, L, H, D] fp32 and lse_parts [n, B, H, L]."""
+    n, B, L, H, D = o_parts.shape
+    out = torch.empty((B, L, H, D), dtype=out_dtype, device=o_parts.device)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=o_parts.device)
+    odt = RA_FP32 if out_dtype == torch.float32 else RA_BF16
+    _check(lib().ra_merge(n, _ptr(o_parts.contiguous()), _ptr(lse_parts.contiguous()), B, L, H, D,
+                          _ptr(out), odt, _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def ra_shard_work_model(seq_len, P, block, layout, causal):
+    """Host closed-form work model: dict of lists (tiles, pairs, visits) per shard."""
+    prm = make_params(1, seq_len, 1, 128, P, block, layout, causal)
+    arr = (ctypes.c_ulonglong * (3 * P))()
+    _check(lib().ra_shard_work_model(ctypes.byref(prm), arr))
+    vals = list(arr)
+    return {"tiles": vals[:P], "pairs": vals[P:2 * P], "visits": vals[2 * P:]}
+
+
+def ra_selftest_timeout(workspace, timeout_us, stream=None):
+    buf = workspace.get(256)
+    _check(lib().ra_selftest_timeout(_ptr(buf), buf.numel(), int(timeout_us), _stream(stream)))
+
+
+class RingAttention(torch.autograd.Function):
+    """autograd wrapper: forward = ra_fwd, backward = ra_bwd (lse saved, scores
+    recomputed)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, P, block, layout, causal, softmax_scale):
+        out, lse = ra_fwd(q, k, v, P, block, layout, causal, softmax_scale)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.cfg = (P, block, layout, causal, softmax_scale)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        P, block, layout, causal, scale = ctx.cfg
+        dq, dk, dv = ra_bwd(q, k, v, out, lse, dout.contiguous(), P, block, layout, causal, scale)
+        return dq, dk, dv, None, None, None, None, None
+
+
+def ring_attention(q, k, v, P, block, layout="contiguous", causal=True, softmax_scale=0.0):
+    return RingAttention.apply(q, k, v, P, block, layout, causal, softmax_scale)

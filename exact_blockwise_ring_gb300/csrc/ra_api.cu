@@ -1,0 +1,403 @@
+// ra_api.cu -- the extern "C" boundary of libra: argument validation, workspace layout,
+// TMA tensor-map encoding, kernel launches, error reporting and the host work model.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+thread_local char g_msg[512] = "";
+
+ra_status_t fail(ra_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ra_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- validation -------------------------------------------------------------------
+ra_status_t check_params(const ra_params_t* p, bool gpu_shapes) {
+  if (!p) return fail(RA_ERR_INVALID_ARG, "params is NULL");
+  if (p->batch < 1 || p->heads < 1 || p->seq_len < 1 || p->P < 1)
+    return fail(RA_ERR_INVALID_ARG, "batch, heads, seq_len and P must be >= 1");
+  if (p->P > 1024) return fail(RA_ERR_INVALID_ARG, "P must be <= 1024");
+  if (p->block < 1) return fail(RA_ERR_INVALID_ARG, "block must be >= 1");
+  if (p->layout != RA_LAYOUT_CONTIGUOUS && p->layout != RA_LAYOUT_STRIPED)
+    return fail(RA_ERR_INVALID_ARG, "layout must be RA_LAYOUT_CONTIGUOUS or RA_LAYOUT_STRIPED");
+  if (p->causal != 0 && p->causal != 1) return fail(RA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (p->seq_len % p->P != 0 || (p->seq_len / p->P) % p->block != 0)
+    return fail(RA_ERR_INVALID_ARG, "seq_len (%lld) must be divisible by P * block (%d * %d)",
+                (long long)p->seq_len, p->P, p->block);
+  if (!gpu_shapes) return RA_OK;
+  if (p->head_dim < 1) return fail(RA_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (p->head_dim != 64 && p->head_dim != 128)
+    return fail(RA_ERR_UNSUPPORTED, "head_dim %d: kernels exist for 64 and 128", p->head_dim);
+  if (p->block != 128 && p->block != 256)
+    return fail(RA_ERR_UNSUPPORTED, "block %d: kernels exist for 128 and 256", p->block);
+  if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale))
+    return fail(RA_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  if (p->n_split < 0 || (p->n_split > 0 && p->P % p->n_split != 0))
+    return fail(RA_ERR_INVALID_ARG, "n_split must be 0 or a divisor of P");
+  const long long elems = (long long)p->batch * p->seq_len * p->heads * p->head_dim;
+  if (elems <= 0 || elems > (1LL << 40))
+    return fail(RA_ERR_INVALID_ARG, "tensor too large");
+  const long long bhl = (long long)p->batch * p->heads * p->seq_len;
+  if (bhl > (1LL << 36)) return fail(RA_ERR_INVALID_ARG, "tensor too large");
+  return RA_OK;
+}
+
+float scale_of(const ra_params_t* p) {
+  return p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)p->head_dim);
+}
+
+int npair_of(const ra_params_t* p) {
+  const int T = (int)(p->seq_len / p->P / kTile);
+  return (T + 1) / 2;
+}
+
+int n_split_of(const ra_params_t* p) {
+  if (p->n_split > 0) return p->n_split;
+  const long long ctas = (long long)p->batch * p->heads * p->P * npair_of(p);
+  if (ctas >= kAutoSplitSMs) return 1;
+  int best = 1;
+  for (int g = 1; g <= p->P; ++g)
+    if (p->P % g == 0 && ctas * g <= 2LL * kAutoSplitSMs) best = g;
+  return best;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t fwd_ws(const ra_params_t* p) {
+  const int g = n_split_of(p);
+  size_t bytes = kWsHeader;
+  if (g > 1) {
+    const size_t o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim * 4;
+    const size_t l = (size_t)p->batch * p->heads * p->seq_len * 4;
+    bytes += round256(g * o) + round256(g * l);
+  }
+  return bytes;
+}
+
+size_t bwd_ws(const ra_params_t* p) {
+  const size_t o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim * 4;
+  const size_t l = (size_t)p->batch * p->heads * p->seq_len * 4;
+  return kWsHeader + round256(o) + round256(l);
+}
+
+// ---- TMA tensor maps --------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// A bf16 [B, L, H, D] tensor viewed as 5-D so that one box is `box_rows` consecutive
+// local rows of one shard and 64 features of one head (128-byte swizzled rows):
+//   striped    dims (D, H, P, n, B): token = local * P + shard
+//   contiguous dims (D, H, n, P, B): token = shard * n + local
+// (strides increase with the dimension index in both views).
+ra_status_t make_rows_map(CUtensorMap* m, const void* base, const ra_params_t* p, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t D = p->head_dim, H = p->heads, P = p->P, B = p->batch;
+  const cuuint64_t L = p->seq_len, n = L / P;
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5], es[5] = {1, 1, 1, 1, 1};
+  dims[0] = D;
+  dims[1] = H;
+  dims[4] = B;
+  strides[0] = D * 2;
+  strides[3] = L * H * D * 2;
+  box[0] = 64;
+  box[1] = 1;
+  box[4] = 1;
+  if (p->layout == RA_LAYOUT_STRIPED) {
+    dims[2] = P;
+    dims[3] = n;
+    strides[1] = H * D * 2;
+    strides[2] = P * H * D * 2;
+    box[2] = 1;
+    box[3] = box_rows;
+  } else {
+    dims[2] = n;
+    dims[3] = P;
+    strides[1] = H * D * 2;
+    strides[2] = n * H * D * 2;
+    box[2] = box_rows;
+    box[3] = 1;
+  }
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return RA_OK;
+}
+
+// ---- host work model (closed forms over the whole ring schedule) -----------------
+void work_model(const ra_params_t* p, unsigned long long* outp) {
+  const int P = p->P, blk = p->block;
+  const long long L = p->seq_len, n = L / P;
+  const long long Tb = n / blk;
+  unsigned long long* tiles = outp;
+  unsigned long long* pairs = outp + P;
+  unsigned long long* visits = outp + 2 * P;
+  for (int i = 0; i < P; ++i) {
+    unsigned long long t = 0, pr = 0, v = 0;
+    const unsigned long long R = (unsigned long long)n;
+    const unsigned long long sum_a = R * (R - 1) / 2;
+    for (int k = 0; k < P; ++k) {
+      const int j = ((i - k) % P + P) % P;
+      if (!p->causal) {
+        t += (unsigned long long)(Tb * Tb);
+        pr += R * n;
+      } else if (p->layout == RA_LAYOUT_STRIPED) {
+        t += (unsigned long long)(Tb * (Tb + 1) / 2);
+        pr += (j <= i) ? sum_a + R : sum_a;
+      } else {
+        for (long long tb = 0; tb < Tb; ++tb) {
+          long long c = (long long)(i - j) * Tb + tb + 1;
+          t += c < 0 ? 0 : (c > Tb ? Tb : c);
+        }
+        pr += (j < i) ? R * n : (j == i ? sum_a + R : 0ull);
+      }
+    }
+    for (long long r = 0; r < n; ++r) {
+      const long long tok = (p->layout == RA_LAYOUT_STRIPED) ? r * P + i : (long long)i * n + r;
+      v += p->causal ? (unsigned long long)(tok / blk + 1) : (unsigned long long)(L / blk);
+    }
+    tiles[i] = t;
+    pairs[i] = pr;
+    visits[i] = v;
+  }
+}
+
+}  // namespace
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+
+const char* ra_status_string(ra_status_t s) {
+  switch (s) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID_ARG: return "RA_ERR_INVALID_ARG";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
+    case RA_ERR_WORKSPACE: return "RA_ERR_WORKSPACE";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA";
+    case RA_ERR_DEVICE_TIMEOUT: return "RA_ERR_DEVICE_TIMEOUT";
+  }
+  return "RA_ERR_UNKNOWN";
+}
+
+const char* ra_last_error_message(void) { return g_msg; }
+
+size_t ra_fwd_workspace_bytes(const ra_params_t* p) {
+  if (check_params(p, true) != RA_OK) return 0;
+  return fwd_ws(p);
+}
+
+size_t ra_bwd_workspace_bytes(const ra_params_t* p) {
+  if (check_params(p, true) != RA_OK) return 0;
+  return bwd_ws(p);
+}
+
+ra_status_t ra_shard_work_model(const ra_params_t* p, unsigned long long* host_out) {
+  ra_status_t s = check_params(p, false);
+  if (s != RA_OK) return s;
+  if (!host_out) return fail(RA_ERR_INVALID_ARG, "host_out is NULL");
+  work_model(p, host_out);
+  return RA_OK;
+}
+
+ra_status_t ra_fwd(const ra_params_t* p, const void* q, const void* k, const void* v, void* out,
+                   int out_dtype, float* lse, unsigned long long* shard_work, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  ra_status_t s = check_params(p, true);
+  if (s != RA_OK) return s;
+  if (!q || !k || !v || !out || !lse) return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (shard_work && (reinterpret_cast<uintptr_t>(shard_work) & 7u))
+    return fail(RA_ERR_INVALID_ARG, "shard_work must be 8-byte aligned");
+  if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
+    return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
+  const size_t need = fwd_ws(p);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,
+                workspace_bytes);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap tq, tk, tv;
+  if ((s = make_rows_map(&tq, q, p, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tk, k, p, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tv, v, p, kTile)) != RA_OK) return s;
+
+  FwdArgs a{};
+  a.B = p->batch;
+  a.H = p->heads;
+  a.D = p->head_dim;
+  a.P = p->P;
+  a.layout = p->layout;
+  a.causal = p->causal;
+  a.block = p->block;
+  a.L = p->seq_len;
+  a.n = (int)(p->seq_len / p->P);
+  a.T = a.n / kTile;
+  a.npair = npair_of(p);
+  a.n_split = n_split_of(p);
+  a.scale_log2 = scale_of(p) * 1.4426950408889634f;
+  a.out = out;
+  a.out_fp32 = out_dtype == RA_FP32;
+  a.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.err = reinterpret_cast<unsigned int*>(ws);
+  if (a.n_split > 1) {
+    const size_t o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim * 4;
+    a.o_part = reinterpret_cast<float*>(ws + kWsHeader);
+    a.lse_part = reinterpret_cast<float*>(ws + kWsHeader + round256(a.n_split * o));
+  }
+  a.shard_work = shard_work;
+  a.wait_limit_ns = kWaitLimitNs;
+  cudaError_t e;
+  if (shard_work) {
+    e = cudaMemsetAsync(shard_work, 0, sizeof(unsigned long long) * 3 * p->P, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(shard_work)");
+  }
+  e = launch_fwd(a, tq, tk, tv, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward kernel launch");
+  if (a.n_split > 1) {
+    e = launch_merge(a.n_split, a.o_part, a.lse_part, a.B, a.L, a.H, a.D, out, a.out_fp32, lse, st);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  }
+  return RA_OK;
+}
+
+ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const void* v,
+                   const void* out, int out_dtype, const float* lse, const void* dout, void* dq,
+                   void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  ra_status_t s = check_params(p, true);
+  if (s != RA_OK) return s;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv)
+    return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
+    return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
+  const size_t need = bwd_ws(p);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,
+                workspace_bytes);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap tq, tk, tv, tdo;
+  if ((s = make_rows_map(&tq, q, p, 64)) != RA_OK) return s;
+  if ((s = make_rows_map(&tk, k, p, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tv, v, p, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tdo, dout, p, 64)) != RA_OK) return s;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim;
+  BwdArgs a{};
+  a.B = p->batch;
+  a.H = p->heads;
+  a.D = p->head_dim;
+  a.P = p->P;
+  a.layout = p->layout;
+  a.causal = p->causal;
+  a.L = p->seq_len;
+  a.n = (int)(p->seq_len / p->P);
+  a.T = a.n / kTile;
+  a.scale = scale_of(p);
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.lse = lse;
+  a.dq_acc = reinterpret_cast<float*>(ws + kWsHeader);
+  a.Dvec = reinterpret_cast<float*>(ws + kWsHeader + round256(o * 4));
+  a.dk = dk;
+  a.dv = dv;
+  a.err = reinterpret_cast<unsigned int*>(ws);
+  a.wait_limit_ns = kWaitLimitNs;
+  cudaError_t e = launch_bwd_pre(out, out_dtype == RA_FP32, dout, const_cast<float*>(a.Dvec),
+                                 a.B, a.L, a.H, a.D, st);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  e = cudaMemsetAsync(a.dq_acc, 0, o * 4, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dq accumulator)");
+  e = launch_bwd(a, tq, tk, tv, tdo, st);
+  if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
+  e = launch_dq_convert(a.dq_acc, dq, a.scale, o, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dq convert launch");
+  return RA_OK;
+}
+
+ra_status_t ra_merge(int n_parts, const float* o_parts, const float* lse_parts, int batch,
+                     int64_t seq_len, int heads, int head_dim, void* out, int out_dtype,
+                     float* lse, void* stream) {
+  if (n_parts < 1 || batch < 1 || seq_len < 1 || heads < 1)
+    return fail(RA_ERR_INVALID_ARG, "n_parts, batch, seq_len, heads must be >= 1");
+  if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0)
+    return fail(RA_ERR_INVALID_ARG, "head_dim must be a multiple of 8 in [8, 256]");
+  if (!o_parts || !lse_parts || !out || !lse) return fail(RA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(o_parts) || !aligned16(out)) return fail(RA_ERR_INVALID_ARG, "misaligned pointer");
+  if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
+    return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
+  if (head_dim % 4 != 0) return fail(RA_ERR_INVALID_ARG, "head_dim must be a multiple of 4");
+  cudaError_t e = launch_merge(n_parts, o_parts, lse_parts, batch, seq_len, heads, head_dim, out,
+                               out_dtype == RA_FP32, lse, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  return RA_OK;
+}
+
+ra_status_t ra_check_error(void* workspace, void* stream) {
+  if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace error word");
+  if (word != 0) {
+    e = cudaMemset(workspace, 0, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace error word");
+    return fail(RA_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%x)", word);
+  }
+  return RA_OK;
+}
+
+ra_status_t ra_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned int timeout_us,
+                                void* stream) {
+  if (!workspace || workspace_bytes < kWsHeader || !aligned16(workspace))
+    return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes", (size_t)kWsHeader);
+  if (timeout_us == 0 || timeout_us > 10000000u)
+    return fail(RA_ERR_INVALID_ARG, "timeout_us must be in [1, 10^7]");
+  cudaError_t e = launch_selftest_timeout(static_cast<unsigned int*>(workspace),
+                                          (uint64_t)timeout_us * 1000ull,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test kernel launch");
+  return RA_OK;
+}
+
+}  // extern "C"

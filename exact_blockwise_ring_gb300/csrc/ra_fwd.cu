@@ -1,0 +1,465 @@
+// ra_fwd.cu -- forward kernel of exact blockwise ring attention on tcgen05 tensor cores.
+//
+// Method (labhub "Ring Attention 論文分析"):
+//   * blockwise attention with an online softmax, section "ブロック単位の分割戦略":
+//     per KV block, new_max = max(max, blockmax), correction = exp(max - new_max),
+//     sum = sum * correction + rowsum(exp(s - new_max)), acc = acc * correction + P V;
+//     finally out = acc / sum;
+//   * ring order, section "リングトポロジーと KV の循環" (and the vanos001 ring diagram):
+//     the queries of shard i visit KV shards (i - k) mod P for k = 0..P-1;
+//   * causal skipping, section "Causal Masking の処理": KV tiles after the query tile
+//     are skipped, the diagonal tile is masked, earlier tiles are not.
+//
+// One CTA owns 256 query rows of one (batch, head, shard): two 128-row tiles that share
+// every K/V tile loaded.  Roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles through an NST-stage ring
+//   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
+//   warp 2      per-shard work counter (one thread), otherwise idle
+//   warps 4-7   softmax of query tile 0 (thread = query row = TMEM lane)
+//   warps 8-11  softmax of query tile 1
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// P (bf16) overwrites the low half of its S columns and is the TMEM A operand of P V.
+// MMA issue order per KV tile n: PV0(n-1), S0(n), PV1(n-1), S1(n), so each softmax
+// warpgroup overlaps the other tile's two MMAs.
+//
+// Online-softmax details: scores are kept in the log2 domain (scale * log2 e folded
+// into one FMA); the running max is refreshed only when a new tile max exceeds it by
+// more than kTau (2^8 headroom), which is exact because the final normalisation and
+// lse use the same stale max.  A row that has seen no visible key keeps max = -inf and
+// takes P = 0 (the -inf guard).  The row sum accumulates fp32 P before P is rounded to
+// bf16 for the tensor core.
+#include <cuda_bf16.h>
+
+#include "ra_internal.h"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr float kTau = 8.0f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NST = (D == 64) ? 4 : 2;       // K/V pipeline stages
+  static constexpr int QB = kTile * D * 2;            // bytes of one Q tile
+  static constexpr int KVB = kTile * D * 2;           // bytes of one K or V tile
+  static constexpr int NCB = D / 64;                  // 128-byte column blocks per row
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * QB;
+  static constexpr int OFF_V = OFF_K + NST * KVB;
+  static constexpr int OFF_BAR = OFF_V + NST * KVB;
+  // barriers: q_full, k_full[NST], v_full[NST], kv_empty[NST], s_full[2], p_full[2],
+  //           o_final[2], drain
+  static constexpr int NBAR = 1 + 3 * NST + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + 1024 alignment slack
+  static constexpr int COL_S = 0;          // + 128 * q
+  static constexpr int COL_O = 256;        // + D * q
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void load_rows(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                          int layout, int d0, int h, int shard, int local0,
+                                          int b) {
+  if (layout == RA_LAYOUT_STRIPED)
+    tma_load_5d(dst, m, bar, d0, h, shard, local0, b);
+  else
+    tma_load_5d(dst, m, bar, d0, h, local0, shard, b);
+}
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+// Work counter for one CTA and its ring steps (closed forms of the tiles it visits).
+__device__ void count_work(const FwdArgs& a, const RingSched& sc, int g) {
+  unsigned long long* tiles = a.shard_work;
+  unsigned long long* pairs = a.shard_work + a.P;
+  unsigned long long* visits = a.shard_work + 2 * a.P;
+  const int i = sc.i;
+  const int Tb = a.n / a.block;
+  unsigned long long n_tiles = 0, n_pairs = 0;
+  // query blocks of `block` rows owned by this CTA: rows [128*t0, 128*(t0+nq)) clipped
+  const int r0 = kTile * sc.t0;
+  int r1 = kTile * (sc.t0 + sc.nq);
+  if (r1 > a.n) r1 = a.n;
+  for (int k = sc.k0; k < sc.k1; ++k) {
+    const int j = sc.j_of(k);
+    for (int tb = r0 / a.block; tb * a.block < r1; ++tb) {
+      if (!a.causal) n_tiles += Tb;
+      else if (a.layout == RA_LAYOUT_STRIPED) n_tiles += tb + 1;
+      else {
+        long long c = (long long)(i - j) * Tb + tb + 1;
+        n_tiles += c < 0 ? 0 : (c > Tb ? Tb : c);
+      }
+    }
+    const unsigned long long R = r1 - r0;
+    const unsigned long long sum_a = R * r0 + R * (R - 1) / 2;   // sum of local rows a
+    if (!a.causal) n_pairs += R * a.n;
+    else if (a.layout == RA_LAYOUT_STRIPED) n_pairs += (j <= i) ? sum_a + R : sum_a;
+    else n_pairs += (j < i) ? R * a.n : (j == i ? sum_a + R : 0ull);
+  }
+  atomicAdd(&tiles[i], n_tiles);
+  atomicAdd(&pairs[i], n_pairs);
+  if (g == 0) {
+    unsigned long long v = 0;
+    for (int r = r0; r < r1; ++r) {
+      const long long tok = (a.layout == RA_LAYOUT_STRIPED) ? (long long)r * a.P + i
+                                                            : (long long)i * a.n + r;
+      v += a.causal ? (unsigned long long)(tok / a.block + 1)
+                    : (unsigned long long)(a.L / a.block);
+    }
+    atomicAdd(&visits[i], v);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    ra_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  constexpr int NST = C::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = sm + C::OFF_Q;
+  uint8_t* sK = sm + C::OFF_K;
+  uint8_t* sV = sm + C::OFF_V;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* kv_empty = v_full + NST;
+  uint64_t* s_full = kv_empty + NST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_final = p_full + 2;
+  uint64_t* drain = o_final + 2;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
+  uint32_t* tmem_slot = misc;
+  volatile uint32_t* abort_flag = misc + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- decode this CTA: heavy work first ---------------------------------------
+  int idx = blockIdx.x;
+  const int BH = a.B * a.H;
+  const int bh = idx % BH;
+  idx /= BH;
+  const int g = idx % a.n_split;
+  idx /= a.n_split;
+  int i, s;
+  if (a.causal && a.layout == RA_LAYOUT_CONTIGUOUS) {
+    const int pos = a.P * a.npair - 1 - idx;
+    i = pos / a.npair;
+    s = pos % a.npair;
+  } else {
+    s = a.npair - 1 - idx / a.P;
+    i = idx % a.P;
+  }
+  const int b = bh / a.H, h = bh % a.H;
+  const int steps = a.P / a.n_split;
+  RingSched sc{i, 2 * s, 2, a.T, a.P, a.layout, a.causal, g * steps, (g + 1) * steps};
+  const int nvalid = (2 * s + 1 < a.T) ? 2 : 1;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = (*(volatile unsigned int*)a.err != 0u) ? 1u : 0u;
+    mbar_init(q_full, 1);
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(&k_full[st], 1);
+      mbar_init(&v_full[st], 1);
+      mbar_init(&kv_empty[st], 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&s_full[q], 1);
+      mbar_init(&p_full[q], 128);
+      mbar_init(&o_final[q], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (*abort_flag) return;   // an earlier CTA gave up: uniform early exit, nothing held
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const WaitCtx wc{abort_flag, a.err, a.wait_limit_ns};
+
+  if (warp == 0) {
+    // ================================================================ producer =====
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_expect_tx(q_full, nvalid * C::QB);
+      for (int q = 0; q < nvalid; ++q)
+        for (int cb = 0; cb < C::NCB; ++cb)
+          load_rows(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h, i,
+                    (2 * s + q) * kTile, b);
+      int n = 0;
+      bool ok = true;
+      for (int k = sc.k0; k < sc.k1 && ok; ++k) {
+        const int j = sc.j_of(k);
+        const int ue = sc.u_end(j);
+        for (int u = 0; u < ue; ++u, ++n) {
+          const int st = n % NST;
+          if (n >= NST && !mbar_wait(&kv_empty[st], ((n / NST) - 1) & 1, wc)) { ok = false; break; }
+          mbar_expect_tx(&k_full[st], C::KVB);
+          for (int cb = 0; cb < C::NCB; ++cb)
+            load_rows(sK + st * C::KVB + cb * kTile * 128, &tmK, &k_full[st], a.layout, cb * 64,
+                      h, j, u * kTile, b);
+          mbar_expect_tx(&v_full[st], C::KVB);
+          for (int cb = 0; cb < C::NCB; ++cb)
+            load_rows(sV + st * C::KVB + cb * kTile * 128, &tmV, &v_full[st], a.layout, cb * 64,
+                      h, j, u * kTile, b);
+        }
+      }
+      // let every copy this thread issued land before the CTA can exit
+      mbar_wait_drain(q_full, 0, a.wait_limit_ns);
+      for (int m = (n > NST ? n - NST : 0); m < n; ++m) {
+        mbar_wait_drain(&k_full[m % NST], (m / NST) & 1, a.wait_limit_ns);
+        mbar_wait_drain(&v_full[m % NST], (m / NST) & 1, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer ===
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      int pend_st[2] = {-1, -1};
+      uint32_t pend_par[2] = {0, 0};
+      int pv_cnt[2] = {0, 0};
+      bool ok = mbar_wait(q_full, 0, wc);
+      tc_fence_after();
+
+      auto issue_pv = [&](int q) -> bool {
+        if (!mbar_wait(&p_full[q], pv_cnt[q] & 1, wc)) return false;
+        if (!mbar_wait(&v_full[pend_st[q]], pend_par[q], wc)) return false;
+        tc_fence_after();
+        const uint32_t vb = v_addr + pend_st[q] * C::KVB;
+        const uint32_t dO = tbase + C::COL_O + q * D;
+        const uint32_t aP = tbase + C::COL_S + q * 128;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(dO, aP + kk * 8, sdesc_mnmajor(vb + kk * 2048, kTile * 128), idPV,
+                  (pv_cnt[q] > 0 || kk > 0) ? 1u : 0u);
+        ++pv_cnt[q];
+        pend_st[q] = -1;
+        return true;
+      };
+
+      int n = 0, prev_st = -1;
+      for (int k = sc.k0; k < sc.k1 && ok; ++k) {
+        const int j = sc.j_of(k);
+        const int ue = sc.u_end(j);
+        for (int u = 0; u < ue && ok; ++u, ++n) {
+          const int st = n % NST;
+          const uint32_t par = (n / NST) & 1;
+          if (!mbar_wait(&k_full[st], par, wc)) { ok = false; break; }
+          tc_fence_after();
+          for (int q = 0; q < 2 && ok; ++q) {
+            if (pend_st[q] >= 0 && !issue_pv(q)) { ok = false; break; }
+            if (sc.cls(q, j, u) != kSkip) {
+              const uint32_t qa = q_addr + q * C::QB, ka = k_addr + st * C::KVB;
+              const uint32_t dS = tbase + C::COL_S + q * 128;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+                umma_ss(dS, sdesc_kmajor(qa + off), sdesc_kmajor(ka + off), idS, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&s_full[q]);
+              pend_st[q] = st;
+              pend_par[q] = par;
+            }
+          }
+          if (ok && n > 0) umma_commit(&kv_empty[prev_st]);
+          prev_st = st;
+        }
+      }
+      for (int q = 0; q < 2 && ok; ++q)
+        if (pend_st[q] >= 0 && !issue_pv(q)) ok = false;
+      if (ok && n > 0) umma_commit(&kv_empty[prev_st]);
+      umma_commit(&o_final[0]);
+      umma_commit(&o_final[1]);
+      umma_commit(drain);
+      if (!ok) mbar_wait_drain(drain, 0, a.wait_limit_ns);
+    }
+  } else if (warp == 2) {
+    if (lane == 0 && a.shard_work != nullptr) count_work(a, sc, g);
+  } else if (warp >= 4) {
+    // ================================================================ softmax ======
+    const int q = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int arow = wq * 32 + lane;              // row inside the 128-row tile
+    const int t = 2 * s + q;
+    const bool valid = t < a.T;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off + C::COL_S + q * 128;
+    const uint32_t tO = tbase + lane_off + C::COL_O + q * D;
+    const float sl2 = a.scale_log2;
+    float m_run = kNegInf, l_run = 0.f;
+    int cnt = 0;
+    bool ok = true;
+    if (valid) {
+      for (int k = sc.k0; k < sc.k1 && ok; ++k) {
+        const int j = sc.j_of(k);
+        const int ue = sc.u_end(j);
+        for (int u = 0; u < ue; ++u) {
+          const int cl = sc.cls(q, j, u);
+          if (cl == kSkip) continue;
+          if (!mbar_wait(&s_full[q], cnt & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          float sv[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tS + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(r[e]);
+          }
+          if (cl == kDiag) {
+            const int lim = arow - ((a.layout == RA_LAYOUT_STRIPED && j > i) ? 1 : 0);
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+              if (e > lim) sv[e] = kNegInf;
+          }
+          float mx[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+#pragma unroll
+          for (int e = 8; e < 128; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
+          const float tmax =
+              fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          const float mt = tmax * sl2;
+          const bool need = mt > m_run + kTau;
+          float corr = 1.f;
+          if (need) {
+            corr = ex2_approx(m_run - mt);
+            l_run *= corr;
+            m_run = mt;
+          }
+          if (cnt > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tO + 32 * c, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+              tmem_st32(tO + 32 * c, r);
+            }
+          }
+          const float mu = (m_run == kNegInf) ? 0.f : m_run;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2_approx(fmaf(sv[32 * c + 2 * e], sl2, -mu));
+              const float p1 = ex2_approx(fmaf(sv[32 * c + 2 * e + 1], sl2, -mu));
+              ls[e & 3] += p0 + p1;
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + 16 * c, pk);
+          }
+          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_full[q]);
+          ++cnt;
+        }
+      }
+    }
+    if (ok && mbar_wait(&o_final[q], 0, wc) && valid) {
+      tc_fence_after();
+      const int loc = t * kTile + arow;
+      const long long tok = (a.layout == RA_LAYOUT_STRIPED) ? (long long)loc * a.P + i
+                                                          : (long long)i * a.n + loc;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : kNegInf;
+      const size_t row = ((size_t)b * a.L + tok) * a.H + h;
+      const size_t lidx = ((size_t)b * a.H + h) * a.L + tok;
+      float* of32 = nullptr;
+      __nv_bfloat16* obf = nullptr;
+      if (a.n_split > 1) {
+        of32 = a.o_part + (size_t)g * a.B * a.L * a.H * D + row * D;
+        a.lse_part[(size_t)g * a.B * a.H * a.L + lidx] = lse_v;
+      } else {
+        if (a.out_fp32) of32 = reinterpret_cast<float*>(a.out) + row * D;
+        else obf = reinterpret_cast<__nv_bfloat16*>(a.out) + row * D;
+        a.lse[lidx] = lse_v;
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + 32 * c, r);
+        tmem_wait_ld();
+        if (of32) {
+          float4* dst = reinterpret_cast<float4*>(of32 + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                 __uint_as_float(r[4 * e + 2]) * inv,
+                                 __uint_as_float(r[4 * e + 3]) * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(obf + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv, __uint_as_float(r[8 * e + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv);
+            dst[e] = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(ra_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)a.B * a.H * a.P * a.npair * a.n_split;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  ra_fwd_kernel<D><<<(unsigned)grid, 384, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, cudaStream_t s) {
+  if (a.D == 64) return launch_fwd_d<64>(a, tq, tk, tv, s);
+  return launch_fwd_d<128>(a, tq, tk, tv, s);
+}
+
+}  // namespace ra

@@ -1,0 +1,174 @@
+/*
+ * ra.h -- C ABI of libra: exact blockwise ring attention (contiguous and striped
+ * layouts) over P virtual shards held on one GPU, for NVIDIA GB300 (sm_103a).
+ *
+ * The method (sources are four web pages on Ring Attention / Striped Attention):
+ *   - "Ring Attention 論文分析" (labhub): blockwise attention with an online softmax
+ *     (section "ブロック単位の分割戦略"), the ring forward (section "リングトポロジーと
+ *     KV の循環"), causal block skipping (section "Causal Masking の処理"), the
+ *     backward with recomputed scores (sections "逆伝播での KV 再循環" and
+ *     "チェックポインティング戦略").
+ *   - "Ring Attention: Sequence Parallelism for Long Context" (vanos001): ring order
+ *     (step k: shard i attends KV shard (i - k) mod P), the striped assignment
+ *     (token r -> shard r mod P, section "The Causal-Mask Problem: Striped
+ *     Attention"), and the per-device work count of section "Worked Demo".
+ *
+ * One call covers all P shards: the pages' per-device ring becomes a schedule inside
+ * one kernel, and a "hop" is a tile load of KV shard (i - k) mod P from device memory.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are row-major.  q, k, v, out, dout, dq, dk, dv are [B, L, H, D] with
+ *     tokens in NATURAL order for both layouts (the shard permutation is internal;
+ *     attention is permutation-equivariant, aibr.jp Striped Attention summary, §3).
+ *     lse is float32 [B, H, L], natural logarithm.
+ *   - All pointers are DEVICE pointers unless stated otherwise, 16-byte aligned.
+ *     The caller owns all memory; the library keeps no allocation between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Compute calls are asynchronous on it.
+ *   - Argument errors are detected on the host, before any launch, and returned as
+ *     RA_ERR_INVALID_ARG / RA_ERR_UNSUPPORTED / RA_ERR_WORKSPACE; nothing is written.
+ *     A failed CUDA runtime call returns RA_ERR_CUDA.  Device-side timeouts (every
+ *     wait in the kernels is bounded) are recorded in the workspace's error word and
+ *     reported by ra_check_error().  No exception or abort crosses this ABI.
+ *   - ra_last_error_message() returns a thread-local text for the last failure.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size or enum value  */
+  RA_ERR_UNSUPPORTED = 2,     /* valid request this build has no kernel for       */
+  RA_ERR_WORKSPACE = 3,       /* workspace null or smaller than *_workspace_bytes */
+  RA_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed                */
+  RA_ERR_DEVICE_TIMEOUT = 5   /* a bounded wait inside a kernel ran out           */
+} ra_status_t;
+
+typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1 } ra_layout_t;
+typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype_t;
+
+/*
+ * Problem description.
+ *   batch, heads     B, H >= 1.
+ *   seq_len          L >= 1, divisible by P * block (the pages assume equal shards,
+ *                    labhub section "長文データの前処理とチャンク割り当て"; there is
+ *                    no padding here).
+ *   head_dim         D in {64, 128}.
+ *   block            the blockwise loop's block size (BPT block_size), {128, 256}.
+ *                    The result does not depend on it beyond rounding order; it sets
+ *                    the unit of the work counter's "tiles".
+ *   P                number of virtual shards (ring length), 1 <= P <= 1024.
+ *   layout           ra_layout_t: CONTIGUOUS (token t -> shard t / (L/P)) or
+ *                    STRIPED (token t -> shard t mod P).
+ *   causal           0 or 1 (key c visible to query r iff c <= r, original positions).
+ *   softmax_scale    > 0, or 0 for 1/sqrt(D).
+ *   n_split          forward only: 1 = one online-softmax state carried over all P
+ *                    ring steps; g > 1 (g divides P) = the ring steps are cut into g
+ *                    groups, each writing a partial (O_g, lse_g) that ra_merge then
+ *                    combines; 0 = let the library choose.
+ */
+typedef struct {
+  int batch;
+  int64_t seq_len;
+  int heads;
+  int head_dim;
+  int block;
+  int P;
+  int layout;
+  int causal;
+  float softmax_scale;
+  int n_split;
+} ra_params_t;
+
+/* Bytes of device workspace ra_fwd / ra_bwd need for `p` (0 if `p` is invalid).
+ * The workspace must be zero-filled before its first use; afterwards the library
+ * keeps its error word consistent (ra_check_error re-zeroes it). */
+size_t ra_fwd_workspace_bytes(const ra_params_t* p);
+size_t ra_bwd_workspace_bytes(const ra_params_t* p);
+
+/*
+ * Forward: out = softmax(scale * q k^T, causal mask) v, lse = log-sum-exp of the
+ * scaled, masked scores, computed ring-wise: the queries of shard i visit KV shards
+ * (i - k) mod P for k = 0..P-1, KV tiles in order inside a shard, merging with an
+ * online softmax (labhub, sections "ブロック単位の分割戦略" and "リングトポロジーと KV
+ * の循環"); causal KV tiles entirely after the query tile are skipped, the diagonal
+ * ones masked (labhub, section "Causal Masking の処理").
+ *   q, k, v      bf16 [B, L, H, D].
+ *   out          [B, L, H, D] of out_dtype (bf16: round to nearest even).
+ *   lse          fp32 [B, H, L]; -inf for a row with no visible key.
+ *   shard_work   NULL, or device uint64 [3][P] overwritten with the per-shard work the
+ *                kernel executed: [0][i] (Q block, KV block) pairs of `block` tokens
+ *                computed for the queries of shard i, [1][i] unmasked (query, key)
+ *                pairs, [2][i] the vanos001 "Worked Demo" unit (per query row, KV
+ *                blocks in natural order holding a visible key).
+ *   workspace    device buffer of >= ra_fwd_workspace_bytes(p) bytes.
+ */
+ra_status_t ra_fwd(const ra_params_t* p, const void* q, const void* k, const void* v,
+                   void* out, int out_dtype, float* lse,
+                   unsigned long long* shard_work,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward (labhub, section "逆伝播での KV 再循環"): with D_r = dO_r . O_r,
+ * P = exp(scale q k^T - lse) (0 where masked), dV = P^T dO, dP = dO V^T,
+ * dS = P * (dP - D) * scale, dQ = dS K, dK = dS^T Q.  Scores are recomputed from
+ * q, k and lse (section "チェックポインティング戦略"); each KV tile stays resident
+ * while the query tiles pass it in ring order (the pages' "dK, dV back to the owner"
+ * becomes on-chip accumulation).
+ *   q, k, v, dout  bf16 [B, L, H, D];  out [B, L, H, D] of out_dtype;  lse from ra_fwd.
+ *   dq, dk, dv     bf16 [B, L, H, D] outputs (fp32 accumulation inside).
+ *   workspace      device buffer of >= ra_bwd_workspace_bytes(p) bytes (holds the
+ *                  fp32 dQ accumulator and D).
+ */
+ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const void* v,
+                   const void* out, int out_dtype, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Merge of normalised partials (the online-softmax correction of labhub section
+ * "ブロック単位の分割戦略", applied to whole partial results):
+ *   lse = ln sum_g exp(lse_g),  out = sum_g exp(lse_g - lse) O_g,
+ * skipping partials with lse_g = -inf; a row whose partials are all -inf gets
+ * out = 0, lse = -inf.
+ *   o_parts    fp32 [n_parts][B, L, H, D];  lse_parts fp32 [n_parts][B, H, L].
+ *   out        [B, L, H, D] of out_dtype;   lse fp32 [B, H, L].
+ * head_dim must be a multiple of 8 and <= 256.
+ */
+ra_status_t ra_merge(int n_parts, const float* o_parts, const float* lse_parts,
+                     int batch, int64_t seq_len, int heads, int head_dim,
+                     void* out, int out_dtype, float* lse, void* stream);
+
+/*
+ * Closed-form per-shard work for `p` in the units of ra_fwd's shard_work, written to
+ * HOST memory host_out[3 * P].  Any block >= 1 dividing L / P is accepted here (the
+ * GPU path needs {128, 256}); with L = 32, P = 4, block = 8, causal, unit [2] gives
+ * the vanos001 demo's 8/16/24/32 (contiguous) and 20/20/20/20 (striped).
+ */
+ra_status_t ra_shard_work_model(const ra_params_t* p, unsigned long long* host_out);
+
+/* Synchronises `stream`, reads the workspace's device error word, re-zeroes it, and
+ * returns RA_ERR_DEVICE_TIMEOUT if a kernel gave up a wait since the last check. */
+ra_status_t ra_check_error(void* workspace, void* stream);
+
+/* Diagnostic for the bounded-wait machinery: launches one CTA that waits on a
+ * barrier nothing arrives on, with a `timeout_us` limit; the kernel records the
+ * timeout in the workspace error word and returns normally (no trap, the context
+ * stays usable).  ra_check_error() then returns RA_ERR_DEVICE_TIMEOUT. */
+ra_status_t ra_selftest_timeout(void* workspace, size_t workspace_bytes,
+                                unsigned int timeout_us, void* stream);
+
+const char* ra_status_string(ra_status_t s);
+const char* ra_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RA_H_ */

@@ -1,0 +1,141 @@
+"""Host-only tests of the C ABI: the library loads, exports every declared symbol, rejects
+bad arguments before any launch, and its closed-form work model matches the oracle's
+enumeration and the printed demo.  No GPU is needed (no compute call reaches CUDA)."""
+
+import ctypes
+import os
+
+import pytest
+
+import oracle
+import exact_blockwise_ring_gb300 as era
+from exact_blockwise_ring_gb300 import api
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(api.LIB_PATH):
+        from exact_blockwise_ring_gb300 import build
+        build.build()
+    return api.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = api.header_symbols()
+    assert "ra_fwd" in names and "ra_bwd" in names and "ra_merge" in names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code, name in api.STATUS.items():
+        assert L.ra_status_string(code).decode() == name
+
+
+def _params(**kw):
+    base = dict(batch=1, seq_len=1024, heads=2, head_dim=128, P=4, block=128, layout=0,
+                causal=1, softmax_scale=0.0, n_split=0)
+    base.update(kw)
+    return api.Params(base["batch"], base["seq_len"], base["heads"], base["head_dim"],
+                      base["block"], base["P"], base["layout"], base["causal"],
+                      base["softmax_scale"], base["n_split"])
+
+
+FAKE = ctypes.c_void_p(1 << 20)      # 16-byte aligned, never dereferenced on these paths
+
+
+def _fwd(L, prm, q=FAKE, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30, odt=0, sw=None):
+    return L.ra_fwd(ctypes.byref(prm), q, FAKE, FAKE, out, odt, lse, sw, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(seq_len=1000), 1),              # not divisible by P * block
+    (dict(batch=0), 1),
+    (dict(heads=0), 1),
+    (dict(P=0), 1),
+    (dict(P=2000, seq_len=2000 * 128), 1),
+    (dict(head_dim=96), 2),               # valid, no kernel
+    (dict(block=64, seq_len=1024), 2),
+    (dict(layout=2), 1),
+    (dict(causal=3), 1),
+    (dict(softmax_scale=-1.0), 1),
+    (dict(softmax_scale=float("inf")), 1),
+    (dict(n_split=3), 1),                 # not a divisor of P
+])
+def test_fwd_rejects_bad_params(L, kw, code):
+    assert _fwd(L, _params(**kw)) == code
+    assert L.ra_last_error_message().decode()
+
+
+def test_fwd_rejects_bad_pointers_and_workspace(L):
+    prm = _params()
+    assert _fwd(L, prm, q=None) == 1
+    assert _fwd(L, prm, out=ctypes.c_void_p((1 << 20) + 8)) == 1
+    assert _fwd(L, prm, odt=7) == 1
+    assert _fwd(L, prm, ws=None) == 3
+    assert _fwd(L, prm, ws_bytes=16) == 3
+    assert _fwd(L, prm, sw=ctypes.c_void_p((1 << 20) + 4)) == 1
+
+
+def test_bwd_rejects_bad_arguments(L):
+    prm = _params()
+    args = [FAKE] * 3 + [FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None]
+    assert L.ra_bwd(ctypes.byref(_params(seq_len=1000)), *args) == 1
+    bad = list(args)
+    bad[7] = None                                            # dq
+    assert L.ra_bwd(ctypes.byref(prm), *bad) == 1
+    bad = list(args)
+    bad[11] = 64                                             # workspace too small
+    assert L.ra_bwd(ctypes.byref(prm), *bad) == 3
+
+
+def test_merge_rejects_bad_arguments(L):
+    assert L.ra_merge(0, FAKE, FAKE, 1, 128, 1, 128, FAKE, 0, FAKE, None) == 1
+    assert L.ra_merge(2, FAKE, FAKE, 1, 128, 1, 12, FAKE, 0, FAKE, None) == 1
+    assert L.ra_merge(2, None, FAKE, 1, 128, 1, 128, FAKE, 0, FAKE, None) == 1
+
+
+def test_workspace_sizes(L):
+    prm = _params(seq_len=32768, heads=32, P=8, n_split=1)
+    assert api.fwd_workspace_bytes(prm) == 256
+    b = api.bwd_workspace_bytes(prm)
+    assert b >= 256 + 32768 * 32 * 128 * 4 + 32 * 32768 * 4
+    assert api.fwd_workspace_bytes(_params(seq_len=1000)) == 0
+    split = api.fwd_workspace_bytes(_params(seq_len=512, heads=2, head_dim=64, n_split=4))
+    assert split >= 256 + 4 * (512 * 2 * 64 * 4 + 2 * 512 * 4)
+
+
+def test_selftest_rejects_bad_arguments(L):
+    assert L.ra_selftest_timeout(None, 256, 100, None) == 3
+    assert L.ra_selftest_timeout(FAKE, 256, 0, None) == 1
+
+
+# ---- host work model against the oracle --------------------------------------------
+
+def test_work_model_reproduces_demo(L):
+    rows = {}
+    for ln in open(os.path.join(GOLDEN, "work_demo.txt")):
+        if ln.strip() and not ln.startswith("#"):
+            f = ln.split()
+            rows[f[0]] = [int(x) for x in f[1:5]]
+    for layout in ("contiguous", "striped"):
+        w = era.ra_shard_work_model(32, 4, 8, layout, True)
+        assert w["visits"] == rows[layout]
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("L_,P,block", [(64, 4, 4), (512, 8, 16), (1024, 2, 128), (2048, 4, 256)])
+def test_work_model_matches_oracle(L, layout, causal, L_, P, block):
+    got = era.ra_shard_work_model(L_, P, block, layout, causal)
+    want = oracle.shard_work(L_, P, block, layout, causal)
+    assert got == want
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(api, "_lib", None)
+    monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "libra.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        api.lib()
