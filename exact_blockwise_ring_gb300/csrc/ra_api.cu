@@ -93,7 +93,7 @@ size_t fwd_ws(const ra_params_t* p) {
 size_t bwd_ws(const ra_params_t* p) {
   const size_t o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim * 4;
   const size_t l = (size_t)p->batch * p->heads * p->seq_len * 4;
-  return kWsHeader + round256(o) + round256(l);
+  return kWsHeader + round256(o) + 2 * round256(l);
 }
 
 // ---- TMA tensor maps --------------------------------------------------------------
@@ -309,6 +309,8 @@ ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const voi
     return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
     return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
+  if (p->head_dim != 128)
+    return fail(RA_ERR_UNSUPPORTED, "backward kernels exist for head_dim 128");
   const size_t need = bwd_ws(p);
   if (!workspace || workspace_bytes < need || !aligned16(workspace))
     return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,
@@ -322,6 +324,10 @@ ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const voi
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim;
+  const size_t l = (size_t)p->batch * p->heads * p->seq_len;
+  float* dq_acc = reinterpret_cast<float*>(ws + kWsHeader);
+  float* Dsm = reinterpret_cast<float*>(ws + kWsHeader + round256(o * 4));
+  float* L2sm = reinterpret_cast<float*>(ws + kWsHeader + round256(o * 4) + round256(l * 4));
   BwdArgs a{};
   a.B = p->batch;
   a.H = p->heads;
@@ -334,15 +340,15 @@ ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const voi
   a.T = a.n / kTile;
   a.scale = scale_of(p);
   a.scale_log2 = a.scale * 1.4426950408889634f;
-  a.lse = lse;
-  a.dq_acc = reinterpret_cast<float*>(ws + kWsHeader);
-  a.Dvec = reinterpret_cast<float*>(ws + kWsHeader + round256(o * 4));
+  a.lse = L2sm;
+  a.Dvec = Dsm;
+  a.dq_acc = dq_acc;
   a.dk = dk;
   a.dv = dv;
   a.err = reinterpret_cast<unsigned int*>(ws);
   a.wait_limit_ns = kWaitLimitNs;
-  cudaError_t e = launch_bwd_pre(out, out_dtype == RA_FP32, dout, const_cast<float*>(a.Dvec),
-                                 a.B, a.L, a.H, a.D, st);
+  cudaError_t e = launch_bwd_pre(out, out_dtype == RA_FP32, dout, lse, Dsm, L2sm, a.B, a.L, a.H,
+                                 a.D, a.P, a.layout, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   e = cudaMemsetAsync(a.dq_acc, 0, o * 4, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dq accumulator)");

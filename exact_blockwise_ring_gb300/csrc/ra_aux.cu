@@ -71,10 +71,14 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) lse[lidx] = tot > 0.f ? mx + logf(tot) : kNegInf;
 }
 
-// D[b, h, tok] = sum_d dO[b, tok, h, d] * O[b, tok, h, d]; one warp per row.
+// Backward preprocess, one warp per row (b, token, h):
+//   D[b, h, shard, local]    = sum_d dO[b, token, h, d] * O[b, token, h, d]
+//   lse2[b, h, shard, local] = lse[b, h, token] * log2(e)
+// written shard-major so the 64 values of one query tile are one contiguous block.
 __global__ void __launch_bounds__(256)
     bwd_pre_kernel(const void* __restrict__ out, int out_fp32, const __nv_bfloat16* __restrict__ dout,
-                   float* __restrict__ Dvec, int B, long long L, int H, int D) {
+                   const float* __restrict__ lse, float* __restrict__ Dsm, float* __restrict__ L2sm,
+                   int B, long long L, int H, int D, int P, int layout) {
   const long long rows = (long long)B * L * H;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -105,7 +109,13 @@ __global__ void __launch_bounds__(256)
     const long long bl = row / H;
     const long long tok = bl % L;
     const int b = (int)(bl / L);
-    Dvec[((size_t)b * H + h) * L + tok] = acc;
+    const long long n = L / P;
+    const long long shard = (layout == RA_LAYOUT_STRIPED) ? tok % P : tok / n;
+    const long long local = (layout == RA_LAYOUT_STRIPED) ? tok / P : tok % n;
+    const size_t bh = (size_t)b * H + h;
+    const size_t dst = (bh * P + shard) * n + local;
+    Dsm[dst] = acc;
+    L2sm[dst] = lse[bh * L + tok] * 1.4426950408889634f;
   }
 }
 
@@ -160,11 +170,13 @@ cudaError_t launch_merge(int n_parts, const float* o_parts, const float* lse_par
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const void* out, int out_fp32, const void* dout, float* Dvec, int B,
-                           int64_t L, int H, int D, cudaStream_t s) {
+cudaError_t launch_bwd_pre(const void* out, int out_fp32, const void* dout, const float* lse,
+                           float* Dsm, float* L2sm, int B, int64_t L, int H, int D, int P,
+                           int layout, cudaStream_t s) {
   const long long rows = (long long)B * L * H;
   bwd_pre_kernel<<<grid_for(rows, 8), 256, 0, s>>>(
-      out, out_fp32, reinterpret_cast<const __nv_bfloat16*>(dout), Dvec, B, L, H, D);
+      out, out_fp32, reinterpret_cast<const __nv_bfloat16*>(dout), lse, Dsm, L2sm, B, L, H, D, P,
+      layout);
   return cudaGetLastError();
 }
 

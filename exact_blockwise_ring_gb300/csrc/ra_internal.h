@@ -78,8 +78,8 @@ struct BwdArgs {
   int n, T;
   float scale;        // softmax scale
   float scale_log2;   // softmax scale * log2(e)
-  const float* lse;   // [B, H, L]
-  const float* Dvec;  // [B, H, L]
+  const float* lse;   // lse * log2(e), shard-major [B, H, P, n]
+  const float* Dvec;  // rowsum(dO * O), shard-major [B, H, P, n]
   float* dq_acc;      // [B, L, H, D] fp32
   void* dk;
   void* dv;
@@ -95,8 +95,9 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMa
 cudaError_t launch_merge(int n_parts, const float* o_parts, const float* lse_parts, int B,
                          int64_t L, int H, int D, void* out, int out_fp32, float* lse,
                          cudaStream_t s);
-cudaError_t launch_bwd_pre(const void* out, int out_fp32, const void* dout, float* Dvec,
-                           int B, int64_t L, int H, int D, cudaStream_t s);
+cudaError_t launch_bwd_pre(const void* out, int out_fp32, const void* dout, const float* lse,
+                           float* Dsm, float* L2sm, int B, int64_t L, int H, int D, int P,
+                           int layout, cudaStream_t s);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, float scale, size_t n,
                               cudaStream_t s);
 cudaError_t launch_selftest_timeout(unsigned int* err, uint64_t limit_ns, cudaStream_t s);

@@ -31,14 +31,14 @@ against things other than itself (a library softmax attention, closed forms,
 finite differences, the pages' printed demo output).  None is "parity unpinned".
 """
 
-from .attention import (attention_fwd, attention_bwd, attention_rows_fwd,
+from .attention import (attention_fwd, attention_bwd, attention_rows_fwd, attention_rows_dq,
                         brute_force_fwd, default_scale)
 from .ring import ring_fwd, ring_partials, merge_partials
 from .work import (shard_of, local_of, shard_tokens, ring_order, shard_work,
                    tile_class)
 
 __all__ = [
-    "attention_fwd", "attention_bwd", "attention_rows_fwd", "brute_force_fwd",
+    "attention_fwd", "attention_bwd", "attention_rows_fwd", "attention_rows_dq", "brute_force_fwd",
     "default_scale", "ring_fwd", "ring_partials", "merge_partials", "shard_of",
     "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class",
 ]

@@ -119,6 +119,28 @@ def attention_rows_fwd(q, k, v, b, h, rows, causal, scale=None):
     return out, lse
 
 
+def attention_rows_dq(q, k, v, dout, b, h, rows, causal, scale=None):
+    """dQ for a few sampled query rows of one (batch, head), O(L*D) per row.
+
+    Row r needs only its own softmax row: dQ_r = sum_c dS[r, c] k_c with
+    dS[r, c] = p[r, c] (dO_r . v_c - dO_r . O_r) * scale.  Returns [len(rows), D].
+    """
+    D = q.shape[3]
+    if scale is None:
+        scale = default_scale(D)
+    out = np.zeros((len(rows), D))
+    for n, r in enumerate(np.asarray(rows, dtype=np.int64)):
+        C = int(r) + 1 if causal else k.shape[1]
+        K = np.asarray(k[b, :C, h, :], dtype=np.float64)
+        V = np.asarray(v[b, :C, h, :], dtype=np.float64)
+        Qr = np.asarray(q[b, r:r + 1, h, :], dtype=np.float64)
+        dOr = np.asarray(dout[b, r:r + 1, h, :], dtype=np.float64)
+        p, _ = _softmax_rows(_scores(Qr, K, int(r), causal, scale))
+        gq, _, _ = _grad_rows(p, Qr, K, V, dOr, scale)
+        out[n] = gq[0]
+    return out
+
+
 def attention_bwd(q, k, v, dout, causal, scale=None):
     """Backward pass by the formulas in the module docstring.
 

@@ -117,6 +117,15 @@ def test_rows_sample_matches_full():
     assert np.max(np.abs(rl - lse[0, 1, rows])) < 1e-14
 
 
+def test_rows_dq_matches_full_backward():
+    q, k, v, dout = _rand(1, 150, 2, 8, seed=14)
+    for causal in (False, True):
+        dq, _, _ = oracle.attention_bwd(q, k, v, dout, causal)
+        rows = [0, 3, 149]
+        got = oracle.attention_rows_dq(q, k, v, dout, 0, 1, rows, causal)
+        assert np.max(np.abs(got - dq[0, rows, 1, :])) < 1e-13
+
+
 def _loss(q, k, v, dout, causal):
     out, _ = oracle.attention_fwd(q, k, v, causal)
     return float(np.sum(out * dout))
