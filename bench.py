@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Benchmark of exact blockwise ring attention on GB300: causal fwd+bwd TFLOP/s.
+
+One step = the whole path on one batch of synthetic input: ra_fwd (forward kernel)
+then the backward's three stages (preprocess, main kernel, dQ finalize).  FLOPs count
+causal-useful work only: per unmasked (query, key) pair 4*D forward and 10*D backward
+(five products, the recompute included).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 32k|262k|1m|8k]
+                  [--layout striped|contiguous] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank runs an independent replica on its own GPU (the
+path has no exchange between GPUs); the rate is all ranks' FLOPs over the slowest
+rank's time.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload (rank 0 only).  Rank 0 prints one JSON line.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal attention fwd+bwd TFLOP/s and % of GB300 dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="32k", choices=["8k", "32k", "262k", "1m"])
+    ap.add_argument("--layout", default=None, choices=["striped", "contiguous"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(3, a.warmup)
+    return a
+
+
+def workload(name, layout):
+    from exact_blockwise_ring_gb300.synthetic import WORKLOADS, SEEDS
+    w = dict(WORKLOADS[name])
+    w["name"] = name
+    w["seed"] = SEEDS[name]
+    w["layout"] = layout or w["layouts"][0]
+    return w
+
+
+def pairs_of(L, causal):
+    return L * (L + 1) // 2 if causal else L * L
+
+
+def flops_of(w, batch_heads=None):
+    bh = batch_heads if batch_heads is not None else w["batch"] * w["heads"]
+    pr = bh * pairs_of(w["seq_len"], w["causal"])
+    D = w["head_dim"]
+    return 4 * D * pr, 10 * D * pr
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_of(w):
+    L, H, D = w["seq_len"], w["heads"], w["head_dim"]
+    tensor_mib = w["batch"] * L * H * D * 2 / 2 ** 20
+    return {"workload": "%s causal fwd+bwd, %s layout" % (w["name"], w["layout"]),
+            "batch": w["batch"], "heads": H, "head_dim": D, "seq_len": L, "P": w["P"],
+            "block": w["block"], "layout": w["layout"], "causal": w["causal"],
+            "l2": "inputs larger than L2 (%.0f MiB per bf16 tensor, L2 129 MB)" % tensor_mib,
+            "flops_per_step": sum(flops_of(w))}
+
+
+# ---------------------------------------------------------------- clocks -----------
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.proc = None
+        self.uuid = uuid
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in out.splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed ------
+def dist_init(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl")
+    return rank, ws, local
+
+
+def dist_max(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle -------
+def oracle_sample(w, tokens, reps=1):
+    """fp64 oracle fwd+bwd on one head of `tokens` tokens of the workload's input
+    distribution.  Returns (seconds per rep, useful TFLOP per rep, cores)."""
+    import numpy as np
+    import oracle
+    from exact_blockwise_ring_gb300.synthetic import make_inputs, to_f64
+    q, k, v, do = to_f64(*make_inputs(1, tokens, 1, w["head_dim"], seed=w["seed"]))
+    cores = len(os.sched_getaffinity(0))
+    t = 0.0
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.attention_fwd(q, k, v, w["causal"])
+        oracle.attention_bwd(q, k, v, do, w["causal"])
+        t += time.perf_counter() - t0
+    pr = pairs_of(tokens, w["causal"])
+    return t / reps, 14 * w["head_dim"] * pr / 1e12, cores
+
+
+CPU_SAMPLE_TOKENS = 32768       # one full head of the 32k workload: ~10-15 s on 16 Grace cores
+REF_STEP_TOKENS = 8192          # one head per reference step
+
+
+def cpu_baseline(w):
+    t, tf, cores = oracle_sample(w, CPU_SAMPLE_TOKENS)
+    return {"value": tf / t, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": "fp64 oracle fwd+bwd, 1 head x %d tokens (causal) of the workload's "
+                      "input distribution, %.1f s; useful-FLOP convention of the GPU line"
+                      % (CPU_SAMPLE_TOKENS, t)}
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "exact_blockwise_ring_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, src_files):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source has
+    not changed since it was captured; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != source_hash(*src_files):
+        return None
+    return e.get("bytes_per_launch_scaled", e.get("bytes_per_launch"))
+
+
+# ---------------------------------------------------------------- our arm ----------
+def run_ours(args, w, rank, world, local):
+    import torch
+    import exact_blockwise_ring_gb300 as era
+    from exact_blockwise_ring_gb300.synthetic import make_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, L, H, D, P, blk = (w["batch"], w["seq_len"], w["heads"], w["head_dim"], w["P"],
+                          w["block"])
+    layout, causal = w["layout"], w["causal"]
+    q, k, v, do = make_inputs(B, L, H, D, w["seed"] + 7919 * rank, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = era.Workspace(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        era.ra_fwd(q, k, v, P, blk, layout, causal, out=out, lse=lse, workspace=ws)
+        era.ra_bwd_stages(q, k, v, out, lse, do, dq, dk, dv, P, blk, layout, causal,
+                          workspace=ws,
+                          between=(lambda i: evs[i + 1].record(stream)) if evs else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ws.check()
+    dist_barrier(world)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(K):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clk = clocks.stop()
+    ws.check()
+    total_ms = t0.elapsed_time(t1)
+    total_ms_max = dist_max(total_ms, world)
+    stage = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(4)]
+    fwd_ms, pre_ms, main_ms, fin_ms = (statistics.mean(x) for x in stage)
+
+    f_fwd, f_bwd = flops_of(w)
+    step_flops = f_fwd + f_bwd
+    ms_per_step = total_ms_max / K
+    value = world * step_flops * K / (total_ms_max * 1e-3) / 1e12
+    pk, pk_kind = peaks()
+    peak_tf = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+
+    # dominant kernel and its roofline (tensor-bound contraction)
+    if main_ms >= fwd_ms:
+        dom, dom_ms, dom_flops, files = "ra_bwd_kernel", main_ms, f_bwd, ("ra_bwd.cu",)
+    else:
+        dom, dom_ms, dom_flops, files = "ra_fwd_kernel", fwd_ms, f_fwd, ("ra_fwd.cu",)
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
+                "peak_kind": "bf16_tflops_sustained of %s" % pk_kind,
+                "traffic": traffic_for(dom, files)}
+
+    # end to end through the public API with host buffers: H2D of the step's inputs from
+    # pinned memory, the two calls, D2H of every result
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+        ho, hl, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                                 for t in (out, lse, dq, dk, dv))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+
+        def e2e_step():
+            for d_, h_ in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            for h_, d_ in ((ho, out), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                h_.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ws.check()
+        e_ms = dist_max(a0.elapsed_time(a1), world)
+        e2e = {"value": round(world * step_flops * K / (e_ms * 1e-3) / 1e12, 2),
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e_ms / K, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w)
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
+                "pct_of_bf16_peak_sustained": round(100.0 * value / world / peak_sus, 2),
+                "config": config_of(w),
+                "stage_ms": {"fwd": round(fwd_ms, 3), "bwd_preprocess": round(pre_ms, 3),
+                             "bwd_main": round(main_ms, 3), "bwd_finalize": round(fin_ms, 3)},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 4 * K, "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- reference arm ----
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    t_steps = []
+    for s in range(args.warmup + args.steps):
+        t, tf, cores = oracle_sample(w, REF_STEP_TOKENS)
+        if s >= args.warmup:
+            t_steps.append(t)
+    total = sum(t_steps)
+    value = tf * len(t_steps) / total
+    sample = ("fp64 oracle fwd+bwd per step: 1 head x %d tokens (causal) of the workload's "
+              "input distribution; useful-FLOP convention of the GPU line" % REF_STEP_TOKENS)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total / len(t_steps), 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    w = workload(args.workload, args.layout)
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores; other ranks exit without work
+        run_reference(args, w, int(os.environ.get("RANK", "0")),
+                      int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    rank, world, local = dist_init(args)
+    try:
+        run_ours(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
