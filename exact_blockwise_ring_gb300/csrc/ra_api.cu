@@ -197,6 +197,9 @@ void work_model(const ra_params_t* p, unsigned long long* outp) {
 }
 
 }  // namespace
+
+void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
 }  // namespace ra
 
 using namespace ra;
@@ -297,37 +300,78 @@ ra_status_t ra_fwd(const ra_params_t* p, const void* q, const void* k, const voi
   return RA_OK;
 }
 
-ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const void* v,
-                   const void* out, int out_dtype, const float* lse, const void* dout, void* dq,
-                   void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace ra {
+namespace {
+
+// Workspace layout of the backward: [header | dQ fp32 [B,L,H,D] | D [B,H,P,n] | lse2].
+struct BwdWs {
+  float* dq_acc;
+  float* Dsm;
+  float* L2sm;
+  size_t o, l;
+};
+
+ra_status_t bwd_common(const ra_params_t* p, void* workspace, size_t workspace_bytes,
+                       BwdWs* w) {
   ra_status_t s = check_params(p, true);
   if (s != RA_OK) return s;
-  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv)
-    return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
-      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
-    return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
   if (p->head_dim != 128)
     return fail(RA_ERR_UNSUPPORTED, "backward kernels exist for head_dim 128");
   const size_t need = bwd_ws(p);
   if (!workspace || workspace_bytes < need || !aligned16(workspace))
     return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,
                 workspace_bytes);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  w->o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim;
+  w->l = (size_t)p->batch * p->heads * p->seq_len;
+  w->dq_acc = reinterpret_cast<float*>(ws + kWsHeader);
+  w->Dsm = reinterpret_cast<float*>(ws + kWsHeader + round256(w->o * 4));
+  w->L2sm = reinterpret_cast<float*>(ws + kWsHeader + round256(w->o * 4) + round256(w->l * 4));
+  return RA_OK;
+}
+
+}  // namespace
+}  // namespace ra
+
+extern "C" {
+
+ra_status_t ra_bwd_preprocess(const ra_params_t* p, const void* out, int out_dtype,
+                              const float* lse, const void* dout, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  BwdWs w;
+  ra_status_t s = bwd_common(p, workspace, workspace_bytes, &w);
+  if (s != RA_OK) return s;
+  if (!out || !lse || !dout) return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(out) || !aligned16(lse) || !aligned16(dout))
+    return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
+    return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_pre(out, out_dtype == RA_FP32, dout, lse, w.Dsm, w.L2sm, p->batch,
+                                 p->seq_len, p->heads, p->head_dim, p->P, p->layout, st);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  e = cudaMemsetAsync(w.dq_acc, 0, w.o * 4, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dq accumulator)");
+  return RA_OK;
+}
+
+ra_status_t ra_bwd_main(const ra_params_t* p, const void* q, const void* k, const void* v,
+                        const void* dout, void* dk, void* dv, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  BwdWs w;
+  ra_status_t s = bwd_common(p, workspace, workspace_bytes, &w);
+  if (s != RA_OK) return s;
+  if (!q || !k || !v || !dout || !dk || !dv) return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dk) ||
+      !aligned16(dv))
+    return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   CUtensorMap tq, tk, tv, tdo;
   if ((s = make_rows_map(&tq, q, p, 64)) != RA_OK) return s;
   if ((s = make_rows_map(&tk, k, p, kTile)) != RA_OK) return s;
   if ((s = make_rows_map(&tv, v, p, kTile)) != RA_OK) return s;
   if ((s = make_rows_map(&tdo, dout, p, 64)) != RA_OK) return s;
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t o = (size_t)p->batch * p->seq_len * p->heads * p->head_dim;
-  const size_t l = (size_t)p->batch * p->heads * p->seq_len;
-  float* dq_acc = reinterpret_cast<float*>(ws + kWsHeader);
-  float* Dsm = reinterpret_cast<float*>(ws + kWsHeader + round256(o * 4));
-  float* L2sm = reinterpret_cast<float*>(ws + kWsHeader + round256(o * 4) + round256(l * 4));
   BwdArgs a{};
   a.B = p->batch;
   a.H = p->heads;
@@ -340,23 +384,49 @@ ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const voi
   a.T = a.n / kTile;
   a.scale = scale_of(p);
   a.scale_log2 = a.scale * 1.4426950408889634f;
-  a.lse = L2sm;
-  a.Dvec = Dsm;
-  a.dq_acc = dq_acc;
+  a.lse = w.L2sm;
+  a.Dvec = w.Dsm;
+  a.dq_acc = w.dq_acc;
   a.dk = dk;
   a.dv = dv;
-  a.err = reinterpret_cast<unsigned int*>(ws);
+  a.err = static_cast<unsigned int*>(workspace);
   a.wait_limit_ns = kWaitLimitNs;
-  cudaError_t e = launch_bwd_pre(out, out_dtype == RA_FP32, dout, lse, Dsm, L2sm, a.B, a.L, a.H,
-                                 a.D, a.P, a.layout, st);
-  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
-  e = cudaMemsetAsync(a.dq_acc, 0, o * 4, st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dq accumulator)");
-  e = launch_bwd(a, tq, tk, tv, tdo, st);
+  cudaError_t e = launch_bwd(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
-  e = launch_dq_convert(a.dq_acc, dq, a.scale, o, st);
+  return RA_OK;
+}
+
+ra_status_t ra_bwd_finalize(const ra_params_t* p, void* dq, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  BwdWs w;
+  ra_status_t s = bwd_common(p, workspace, workspace_bytes, &w);
+  if (s != RA_OK) return s;
+  if (!dq || !aligned16(dq)) return fail(RA_ERR_INVALID_ARG, "dq must be a 16-byte aligned pointer");
+  cudaError_t e = launch_dq_convert(w.dq_acc, dq, scale_of(p), w.o,
+                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "dq convert launch");
   return RA_OK;
+}
+
+ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const void* v,
+                   const void* out, int out_dtype, const float* lse, const void* dout, void* dq,
+                   void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  // validate everything before the first launch
+  BwdWs w;
+  ra_status_t s = bwd_common(p, workspace, workspace_bytes, &w);
+  if (s != RA_OK) return s;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv)
+    return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
+    return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
+  s = ra_bwd_preprocess(p, out, out_dtype, lse, dout, workspace, workspace_bytes, stream);
+  if (s != RA_OK) return s;
+  s = ra_bwd_main(p, q, k, v, dout, dk, dv, workspace, workspace_bytes, stream);
+  if (s != RA_OK) return s;
+  return ra_bwd_finalize(p, dq, workspace, workspace_bytes, stream);
 }
 
 ra_status_t ra_merge(int n_parts, const float* o_parts, const float* lse_parts, int batch,

@@ -102,4 +102,7 @@ cudaError_t launch_dq_convert(const float* dq_acc, void* dq, float scale, size_t
                               cudaStream_t s);
 cudaError_t launch_selftest_timeout(unsigned int* err, uint64_t limit_ns, cudaStream_t s);
 
+// Sets the text ra_last_error_message() returns on this thread.
+void set_last_error_message(const char* msg);
+
 }  // namespace ra

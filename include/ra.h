@@ -133,6 +133,26 @@ ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const voi
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The three stages ra_bwd runs, callable one by one (same kernels, same workspace):
+ *   ra_bwd_preprocess  D = rowsum(dO * O) and lse * log2(e), both stored shard-major
+ *                      ([B, H, P, L/P] fp32) in the workspace; zeroes the fp32 dQ
+ *                      accumulator (labhub, "逆伝播での KV 再循環": the D vector).
+ *   ra_bwd_main        the ring backward proper: writes dk, dv (bf16) and accumulates
+ *                      unscaled dQ into the workspace.  Needs the preprocess results.
+ *   ra_bwd_finalize    dq = bf16(scale * accumulated dQ).
+ * Arguments have the meaning given for ra_bwd; the same workspace must be passed to all
+ * three, in this order, on one stream.
+ */
+ra_status_t ra_bwd_preprocess(const ra_params_t* p, const void* out, int out_dtype,
+                              const float* lse, const void* dout, void* workspace,
+                              size_t workspace_bytes, void* stream);
+ra_status_t ra_bwd_main(const ra_params_t* p, const void* q, const void* k, const void* v,
+                        const void* dout, void* dk, void* dv, void* workspace,
+                        size_t workspace_bytes, void* stream);
+ra_status_t ra_bwd_finalize(const ra_params_t* p, void* dq, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * Merge of normalised partials (the online-softmax correction of labhub section
  * "ブロック単位の分割戦略", applied to whole partial results):
  *   lse = ln sum_g exp(lse_g),  out = sum_g exp(lse_g - lse) O_g,
@@ -153,6 +173,30 @@ ra_status_t ra_merge(int n_parts, const float* o_parts, const float* lse_parts,
  * the vanos001 demo's 8/16/24/32 (contiguous) and 20/20/20/20 (striped).
  */
 ra_status_t ra_shard_work_model(const ra_params_t* p, unsigned long long* host_out);
+
+/*
+ * Backward without a workspace, for callers that cannot allocate device memory: a
+ * plugin whose host runtime hands it tensors and a stream but no allocator, or a
+ * latency-critical caller that may not call cudaMalloc on its hot path (the call can
+ * synchronise the device and its cost is unbounded).  The pages have no counterpart of
+ * this entry point; it is a deployment convenience.
+ *   Same computation and arguments as ra_bwd, minus the workspace: the scratch (error
+ *   word, fp32 dQ accumulator, D, lse * log2(e)) lives in one 64 MiB array of device
+ *   memory inside the library, which every GPU that loads the library holds until the
+ *   process exits.  Problems whose ra_bwd_workspace_bytes() exceeds 64 MiB are rejected
+ *   with RA_ERR_WORKSPACE (roughly B * L * H above 128K rows at head_dim 128).
+ *   The first call on a device looks up the array's device address with that device
+ *   current (set-up); make that first call before any stream capture.
+ *   Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   All calls share the one array, and it keeps the last call's contents: each call
+ *   clears the error word and zeroes the dQ accumulator itself.  Calls that overlap on
+ *   the GPU (two streams, or two threads) race on the array and corrupt each other;
+ *   serialise them.  A device-side timeout of one call is cleared by the next call, so
+ *   it is not reported through this entry point (use ra_bwd + ra_check_error for that).
+ */
+ra_status_t ra_bwd_noalloc(const ra_params_t* p, const void* q, const void* k, const void* v,
+                           const void* out, int out_dtype, const float* lse, const void* dout,
+                           void* dq, void* dk, void* dv, void* stream);
 
 /* Synchronises `stream`, reads the workspace's device error word, re-zeroes it, and
  * returns RA_ERR_DEVICE_TIMEOUT if a kernel gave up a wait since the last check. */
