@@ -5,9 +5,9 @@ The computation lives in libra.so (C ABI: include/ra.h), built from csrc/ by
 """
 
 from .api import (LAYOUTS, Params, RaError, RingAttention, Workspace, bwd_workspace_bytes,
-                  fwd_workspace_bytes, header_symbols, lib, make_params, ra_bwd, ra_fwd,
+                  fwd_workspace_bytes, header_symbols, lib, make_params, ra_bwd, ra_bwd_stages, ra_fwd,
                   ra_merge, ra_selftest_timeout, ra_shard_work_model, ring_attention)
 
 __all__ = ["LAYOUTS", "Params", "RaError", "RingAttention", "Workspace", "bwd_workspace_bytes",
-           "fwd_workspace_bytes", "header_symbols", "lib", "make_params", "ra_bwd", "ra_fwd",
+           "fwd_workspace_bytes", "header_symbols", "lib", "make_params", "ra_bwd", "ra_bwd_stages", "ra_fwd",
            "ra_merge", "ra_selftest_timeout", "ra_shard_work_model", "ring_attention"]

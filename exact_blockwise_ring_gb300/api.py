@@ -47,6 +47,11 @@ _SIGS = {
                               ctypes.c_size_t, _P]),
     "ra_bwd": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, ctypes.c_int, _P, _P, _P,
                               _P, _P, _P, ctypes.c_size_t, _P]),
+    "ra_bwd_preprocess": (ctypes.c_int, [ctypes.POINTER(Params), _P, ctypes.c_int, _P, _P, _P,
+                                         ctypes.c_size_t, _P]),
+    "ra_bwd_main": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, _P, _P, _P,
+                                   ctypes.c_size_t, _P]),
+    "ra_bwd_finalize": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, ctypes.c_size_t, _P]),
     "ra_merge": (ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                 ctypes.c_int, _P, ctypes.c_int, _P, _P]),
     "ra_shard_work_model": (ctypes.c_int, [ctypes.POINTER(Params),
@@ -190,6 +195,35 @@ def ra_bwd(q, k, v, out, lse, dout, P, block, layout="contiguous", causal=True,
     _check(lib().ra_bwd(ctypes.byref(prm), _ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse),
                         _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(buf), buf.numel(),
                         _stream(stream)))
+    return dq, dk, dv
+
+
+def ra_bwd_stages(q, k, v, out, lse, dout, dq, dk, dv, P, block, layout="contiguous",
+                  causal=True, softmax_scale=0.0, workspace=None, stream=None, between=None):
+    """The backward as its three C-ABI stages (preprocess, main, finalize).
+
+    ``between(i)`` (optional) is called before stage i (0, 1, 2) and after the last
+    (i = 3), e.g. to record CUDA events around each stage."""
+    B, L, H, D = _check_qkv(q, k, v, dout)
+    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, 0)
+    odt = RA_FP32 if out.dtype == torch.float32 else RA_BF16
+    ws = workspace or default_workspace(q.device)
+    buf = ws.get(max(bwd_workspace_bytes(prm), 256))
+    st = _stream(stream)
+    h = lib()
+    if between:
+        between(0)
+    _check(h.ra_bwd_preprocess(ctypes.byref(prm), _ptr(out), odt, _ptr(lse), _ptr(dout),
+                               _ptr(buf), buf.numel(), st))
+    if between:
+        between(1)
+    _check(h.ra_bwd_main(ctypes.byref(prm), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk),
+                         _ptr(dv), _ptr(buf), buf.numel(), st))
+    if between:
+        between(2)
+    _check(h.ra_bwd_finalize(ctypes.byref(prm), _ptr(dq), _ptr(buf), buf.numel(), st))
+    if between:
+        between(3)
     return dq, dk, dv
 
 

@@ -10,14 +10,16 @@
 // TMEM and leave once.  dQ partials are added into an fp32 accumulator in global memory.
 //
 // One CTA = 128 keys (tile u of shard j) of one (batch, head).  Query tiles are 64 rows.
-// Roles (384 threads):
+// Roles (512 threads):
 //   warp 0      producer: K, V once (TMA); per query tile Q, dO (TMA) and its 64 lse
 //               (log2 domain) and D values (bulk copies from the shard-major arrays the
 //               preprocess kernel wrote)
 //   warp 1      TMEM allocator and tcgen05.mma issuer
-//   warps 4-7   thread = key row: P^T = exp2(S^T*c - lse2), dS^T = P^T (dP^T - D), both
-//               rounded to bf16 into 128-byte-swizzled shared tiles; finally dK, dV out
-//   warps 8-11  thread = feature d: dQ^T tile from TMEM -> fp32 reductions into dq_acc
+//   warps 4-11  two warpgroups, thread = key row, warpgroup g takes query columns
+//               [32g, 32g+32): P^T = exp2(S^T*c - lse2), dS^T = P^T (dP^T - D), both
+//               rounded to bf16 into 128-byte-swizzled shared tiles; at the end
+//               warpgroup 0 writes dV and warpgroup 1 writes dK
+//   warps 12-15 thread = feature d: dQ^T tile from TMEM -> fp32 reductions into dq_acc
 // MMAs per query tile m (M = 128 rows of TMEM lanes):
 //   S^T  = K Q^T      A K-major smem,    B K-major smem    (N = 64)
 //   dP^T = V dO^T     A K-major,         B K-major         (N = 64)
@@ -120,7 +122,7 @@ struct BwdSched {
   }
 };
 
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     ra_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs a) {
@@ -153,11 +155,11 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- decode: heavy KV tiles (early positions) first ----------------------------
-  int idx = blockIdx.x;
-  const int BH = a.B * a.H;
-  const int bh = idx % BH;
-  idx /= BH;
+  // ---- decode: one (batch, head) after another (the resident CTAs then share that
+  // head's Q, dO and dQ accumulator in L2); inside a head, heavy KV tiles first --------
+  const int per_bh = a.P * a.T;
+  const int bh = blockIdx.x / per_bh;
+  int idx = blockIdx.x % per_bh;
   int j, u;
   if (a.layout == RA_LAYOUT_STRIPED || !a.causal) {
     u = idx / a.P;
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&q_empty[st], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(ds_ready, 128);
+    mbar_init(ds_ready, 256);
     mbar_init(&ds_free[0], 1);
     mbar_init(&ds_free[1], 1);
     mbar_init(dq_full, 1);
@@ -302,12 +304,14 @@ __global__ void __launch_bounds__(384, 1)
       umma_commit(drain);
       if (!ok) mbar_wait_drain(drain, 0, a.wait_limit_ns);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ================================================================ key rows =====
     const int wq = warp & 3;
+    const int half = (warp - 4) >> 2;             // query columns [32*half, 32*half + 32)
     const int brow = wq * 32 + lane;              // key row in the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tbase + lane_off + C::COL_S, tDP = tbase + lane_off + C::COL_DP;
+    const uint32_t tS = tbase + lane_off + C::COL_S + 32 * half;
+    const uint32_t tDP = tbase + lane_off + C::COL_DP + 32 * half;
     const float sl2 = a.scale_log2;
     bool ok = true;
     int m = 0;
@@ -320,40 +324,28 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        uint32_t sr[64], pr[64];
-        {
-          uint32_t r[32];
-          tmem_ld32(tS, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sr[e] = r[e];
-          tmem_ld32(tS + 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sr[32 + e] = r[e];
-          tmem_ld32(tDP, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[e] = r[e];
-          tmem_ld32(tDP + 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[32 + e] = r[e];
-          tmem_wait_ld();
-        }
-        const float* lse2 = sLD + st * (2 * BQ);
+        uint32_t sr[32], pr[32];
+        tmem_ld32(tS, sr);
+        tmem_ld32(tDP, pr);
+        tmem_wait_ld();
+        const float* lse2 = sLD + st * (2 * BQ) + 32 * half;
         const float* dv = lse2 + BQ;
         const long long dl = a.causal ? sc.delta(i, t) : 1000000LL;
-        // visible iff col - brow + delta >= 0  ->  col >= brow - delta
-        const long long lim = (long long)brow - dl;
+        // visible iff col - brow + delta >= 0  ->  col >= brow - delta (col = 32*half + c)
+        const long long lim = (long long)brow - dl - 32 * half;
         if (m >= 2 && !mbar_wait(&ds_free[m & 1], ((m >> 1) - 1) & 1, wc)) { ok = false; break; }
         uint8_t* prow = sPT + (m & 1) * C::SB + brow * 128;
         uint8_t* drow = sDS + (m & 1) * C::SB + brow * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int c8l = 0; c8l < 4; ++c8l) {
+          const int c8 = 4 * half + c8l;
           uint32_t pw[4], dw[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
             float p[2], ds[2];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const int c = c8 * 8 + e2 * 2 + h2;
+              const int c = c8l * 8 + e2 * 2 + h2;
               const float s = __uint_as_float(sr[c]);
               float pv = ex2_approx(fmaf(s, sl2, -lse2[c]));
               if ((long long)c < lim) pv = 0.f;
@@ -382,8 +374,8 @@ __global__ void __launch_bounds__(384, 1)
       __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(a.dv) + row * D_;
       __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(a.dk) + row * D_;
       const bool any = m > 0;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
+      {
+        const int which = half;
         const uint32_t tcol = tbase + lane_off + (which ? C::COL_DK : C::COL_DV);
         const float mul = which ? a.scale : 1.f;
         __nv_bfloat16* dst = which ? dkp : dvp;
@@ -404,7 +396,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ================================================================ dQ drain =====
     const int wq = warp & 3;
     const int d = wq * 32 + lane;                 // feature owned by this thread
@@ -455,7 +447,7 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMa
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.B * a.H * a.P * a.T;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ra_bwd_kernel<<<(unsigned)grid, 384, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  ra_bwd_kernel<<<(unsigned)grid, 512, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 

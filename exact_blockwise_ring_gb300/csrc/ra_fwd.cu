@@ -148,11 +148,11 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- decode this CTA: heavy work first ---------------------------------------
-  int idx = blockIdx.x;
-  const int BH = a.B * a.H;
-  const int bh = idx % BH;
-  idx /= BH;
+  // ---- decode this CTA: one (batch, head) after another so that the CTAs resident at
+  // any time share that head's K/V in L2; inside a head, heavy work first --------------
+  const int per_bh = a.n_split * a.P * a.npair;
+  const int bh = blockIdx.x / per_bh;
+  int idx = blockIdx.x % per_bh;
   const int g = idx % a.n_split;
   idx /= a.n_split;
   int i, s;

@@ -259,6 +259,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Warpgroup register reallocation: the launch gives every thread the same count; the
+// producer/MMA warpgroup hands registers back and the math warpgroups take them.
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- math -------------
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
