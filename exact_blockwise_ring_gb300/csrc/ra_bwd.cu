@@ -339,18 +339,25 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int c8l = 0; c8l < 4; ++c8l) {
           const int c8 = 4 * half + c8l;
+          // the 8 columns' lse2 and D: two 16-byte broadcast loads each
+          float lv[8], dd[8];
+          *reinterpret_cast<float4*>(&lv[0]) = reinterpret_cast<const float4*>(lse2)[2 * c8l];
+          *reinterpret_cast<float4*>(&lv[4]) = reinterpret_cast<const float4*>(lse2)[2 * c8l + 1];
+          *reinterpret_cast<float4*>(&dd[0]) = reinterpret_cast<const float4*>(dv)[2 * c8l];
+          *reinterpret_cast<float4*>(&dd[4]) = reinterpret_cast<const float4*>(dv)[2 * c8l + 1];
           uint32_t pw[4], dw[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
             float p[2], ds[2];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const int c = c8l * 8 + e2 * 2 + h2;
+              const int cl = e2 * 2 + h2;
+              const int c = c8l * 8 + cl;
               const float s = __uint_as_float(sr[c]);
-              float pv = ex2_approx(fmaf(s, sl2, -lse2[c]));
+              float pv = ex2_approx(fmaf(s, sl2, -lv[cl]));
               if ((long long)c < lim) pv = 0.f;
               p[h2] = pv;
-              ds[h2] = pv * (__uint_as_float(pr[c]) - dv[c]);
+              ds[h2] = pv * (__uint_as_float(pr[c]) - dd[cl]);
             }
             pw[e2] = pack_bf16x2(p[0], p[1]);
             dw[e2] = pack_bf16x2(ds[0], ds[1]);

@@ -12,20 +12,23 @@
 //
 // One CTA owns 256 query rows of one (batch, head, shard): two 128-row tiles that share
 // every K/V tile loaded.  Roles (384 threads):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles through an NST-stage ring
+//   warp 0      TMA producer of Q (once) and of the K tiles (NK-stage ring)
 //   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
 //   warp 2      per-shard work counter (one thread), otherwise idle
+//   warp 3      TMA producer of the V tiles (NV-stage ring)
 //   warps 4-7   softmax of query tile 0 (thread = query row = TMEM lane)
 //   warps 8-11  softmax of query tile 1
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // P (bf16) overwrites the low half of its S columns and is the TMEM A operand of P V.
 // MMA issue order per KV tile n: PV0(n-1), S0(n), PV1(n-1), S1(n), so each softmax
-// warpgroup overlaps the other tile's two MMAs.
+// warpgroup overlaps the other tile's two MMAs.  K and V have separate rings: a K tile is
+// released as soon as both S MMAs that read it are done, a V tile after both PV MMAs.
 //
-// Online-softmax details: scores are kept in the log2 domain (scale * log2 e folded
-// into one FMA); the running max is refreshed only when a new tile max exceeds it by
-// more than kTau (2^8 headroom), which is exact because the final normalisation and
-// lse use the same stale max.  A row that has seen no visible key keeps max = -inf and
+// Online-softmax details: exponentials are taken in base 2 with the running max m kept in
+// raw score units, P = exp2((s - m) * scale * log2 e), so the maximum element gets exactly
+// 1; m is refreshed only when a new tile max exceeds it by more than kTau in the log2
+// domain (2^8 headroom), which is exact because the final normalisation and lse use the
+// same stale max.  A row that has seen no visible key keeps max = -inf and
 // takes P = 0 (the -inf guard).  The row sum accumulates fp32 P before P is rounded to
 // bf16 for the tensor core.
 #include <cuda_bf16.h>
@@ -42,17 +45,18 @@ constexpr float kNegInf = -__builtin_huge_valf();
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NST = (D == 64) ? 4 : 2;       // K/V pipeline stages
+  static constexpr int NK = (D == 64) ? 4 : 3;        // K pipeline stages
+  static constexpr int NV = (D == 64) ? 4 : 2;        // V pipeline stages
   static constexpr int QB = kTile * D * 2;            // bytes of one Q tile
   static constexpr int KVB = kTile * D * 2;           // bytes of one K or V tile
   static constexpr int NCB = D / 64;                  // 128-byte column blocks per row
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * QB;
-  static constexpr int OFF_V = OFF_K + NST * KVB;
-  static constexpr int OFF_BAR = OFF_V + NST * KVB;
-  // barriers: q_full, k_full[NST], v_full[NST], kv_empty[NST], s_full[2], p_full[2],
-  //           o_final[2], drain
-  static constexpr int NBAR = 1 + 3 * NST + 7;
+  static constexpr int OFF_V = OFF_K + NK * KVB;
+  static constexpr int OFF_BAR = OFF_V + NV * KVB;
+  // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
+  //           p_full[2], o_final[2], drain
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + 1024 alignment slack
   static constexpr int COL_S = 0;          // + 128 * q
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(384, 1)
     ra_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
   using C = FwdCfg<D>;
-  constexpr int NST = C::NST;
+  constexpr int NK = C::NK, NV = C::NV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -135,9 +139,10 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + NST;
-  uint64_t* kv_empty = v_full + NST;
-  uint64_t* s_full = kv_empty + NST;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_final = p_full + 2;
   uint64_t* drain = o_final + 2;
@@ -172,10 +177,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     *abort_flag = (*(volatile unsigned int*)a.err != 0u) ? 1u : 0u;
     mbar_init(q_full, 1);
-    for (int st = 0; st < NST; ++st) {
+    for (int st = 0; st < NK; ++st) {
       mbar_init(&k_full[st], 1);
+      mbar_init(&k_empty[st], 1);
+    }
+    for (int st = 0; st < NV; ++st) {
       mbar_init(&v_full[st], 1);
-      mbar_init(&kv_empty[st], 1);
+      mbar_init(&v_empty[st], 1);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&s_full[q], 1);
@@ -197,41 +205,43 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tbase = *tmem_slot;
   const WaitCtx wc{abort_flag, a.err, a.wait_limit_ns};
 
-  if (warp == 0) {
-    // ================================================================ producer =====
+  if (warp == 0 || warp == 3) {
+    // ================================================================ producers ====
+    // warp 0: Q once, then K tiles; warp 3: V tiles.  Both walk the same item sequence.
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_expect_tx(q_full, nvalid * C::QB);
-      for (int q = 0; q < nvalid; ++q)
-        for (int cb = 0; cb < C::NCB; ++cb)
-          load_rows(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h, i,
-                    (2 * s + q) * kTile, b);
+      const bool is_k = warp == 0;
+      const int NS = is_k ? NK : NV;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = is_k ? sK : sV;
+      const CUtensorMap* tm = is_k ? &tmK : &tmV;
+      tma_prefetch_desc(tm);
+      if (is_k) {
+        tma_prefetch_desc(&tmQ);
+        mbar_expect_tx(q_full, nvalid * C::QB);
+        for (int q = 0; q < nvalid; ++q)
+          for (int cb = 0; cb < C::NCB; ++cb)
+            load_rows(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h, i,
+                      (2 * s + q) * kTile, b);
+      }
       int n = 0;
       bool ok = true;
       for (int k = sc.k0; k < sc.k1 && ok; ++k) {
         const int j = sc.j_of(k);
         const int ue = sc.u_end(j);
         for (int u = 0; u < ue; ++u, ++n) {
-          const int st = n % NST;
-          if (n >= NST && !mbar_wait(&kv_empty[st], ((n / NST) - 1) & 1, wc)) { ok = false; break; }
-          mbar_expect_tx(&k_full[st], C::KVB);
+          const int st = n % NS;
+          if (n >= NS && !mbar_wait(&empty[st], ((n / NS) - 1) & 1, wc)) { ok = false; break; }
+          mbar_expect_tx(&full[st], C::KVB);
           for (int cb = 0; cb < C::NCB; ++cb)
-            load_rows(sK + st * C::KVB + cb * kTile * 128, &tmK, &k_full[st], a.layout, cb * 64,
-                      h, j, u * kTile, b);
-          mbar_expect_tx(&v_full[st], C::KVB);
-          for (int cb = 0; cb < C::NCB; ++cb)
-            load_rows(sV + st * C::KVB + cb * kTile * 128, &tmV, &v_full[st], a.layout, cb * 64,
-                      h, j, u * kTile, b);
+            load_rows(ring + st * C::KVB + cb * kTile * 128, tm, &full[st], a.layout, cb * 64, h,
+                      j, u * kTile, b);
         }
       }
       // let every copy this thread issued land before the CTA can exit
-      mbar_wait_drain(q_full, 0, a.wait_limit_ns);
-      for (int m = (n > NST ? n - NST : 0); m < n; ++m) {
-        mbar_wait_drain(&k_full[m % NST], (m / NST) & 1, a.wait_limit_ns);
-        mbar_wait_drain(&v_full[m % NST], (m / NST) & 1, a.wait_limit_ns);
-      }
+      if (is_k) mbar_wait_drain(q_full, 0, a.wait_limit_ns);
+      for (int m = (n > NS ? n - NS : 0); m < n; ++m)
+        mbar_wait_drain(&full[m % NS], (m / NS) & 1, a.wait_limit_ns);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer ===
@@ -239,7 +249,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      int pend_st[2] = {-1, -1};
+      int pend_st[2] = {-1, -1};      // V stage of the item whose PV is still to be issued
       uint32_t pend_par[2] = {0, 0};
       int pv_cnt[2] = {0, 0};
       bool ok = mbar_wait(q_full, 0, wc);
@@ -261,19 +271,18 @@ __global__ void __launch_bounds__(384, 1)
         return true;
       };
 
-      int n = 0, prev_st = -1;
+      int n = 0;
       for (int k = sc.k0; k < sc.k1 && ok; ++k) {
         const int j = sc.j_of(k);
         const int ue = sc.u_end(j);
         for (int u = 0; u < ue && ok; ++u, ++n) {
-          const int st = n % NST;
-          const uint32_t par = (n / NST) & 1;
-          if (!mbar_wait(&k_full[st], par, wc)) { ok = false; break; }
+          const int kst = n % NK, vst = n % NV;
+          if (!mbar_wait(&k_full[kst], (n / NK) & 1, wc)) { ok = false; break; }
           tc_fence_after();
           for (int q = 0; q < 2 && ok; ++q) {
             if (pend_st[q] >= 0 && !issue_pv(q)) { ok = false; break; }
             if (sc.cls(q, j, u) != kSkip) {
-              const uint32_t qa = q_addr + q * C::QB, ka = k_addr + st * C::KVB;
+              const uint32_t qa = q_addr + q * C::QB, ka = k_addr + kst * C::KVB;
               const uint32_t dS = tbase + C::COL_S + q * 128;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
@@ -281,17 +290,18 @@ __global__ void __launch_bounds__(384, 1)
                 umma_ss(dS, sdesc_kmajor(qa + off), sdesc_kmajor(ka + off), idS, kk > 0 ? 1u : 0u);
               }
               umma_commit(&s_full[q]);
-              pend_st[q] = st;
-              pend_par[q] = par;
+              pend_st[q] = vst;
+              pend_par[q] = (n / NV) & 1;
             }
           }
-          if (ok && n > 0) umma_commit(&kv_empty[prev_st]);
-          prev_st = st;
+          if (!ok) break;
+          umma_commit(&k_empty[kst]);                       // both S MMAs of item n issued
+          if (n > 0) umma_commit(&v_empty[(n - 1) % NV]);    // every PV of item n-1 issued
         }
       }
       for (int q = 0; q < 2 && ok; ++q)
         if (pend_st[q] >= 0 && !issue_pv(q)) ok = false;
-      if (ok && n > 0) umma_commit(&kv_empty[prev_st]);
+      if (ok && n > 0) umma_commit(&v_empty[(n - 1) % NV]);
       umma_commit(&o_final[0]);
       umma_commit(&o_final[1]);
       umma_commit(drain);
@@ -310,7 +320,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tbase + lane_off + C::COL_S + q * 128;
     const uint32_t tO = tbase + lane_off + C::COL_O + q * D;
     const float sl2 = a.scale_log2;
-    float m_run = kNegInf, l_run = 0.f;
+    const float tau_raw = kTau / sl2;           // rescale threshold in raw score units
+    float m_run = kNegInf, l_run = 0.f;         // running max (raw units) and row sum
     int cnt = 0;
     bool ok = true;
     if (valid) {
@@ -337,21 +348,25 @@ __global__ void __launch_bounds__(384, 1)
             for (int e = 0; e < 128; ++e)
               if (e > lim) sv[e] = kNegInf;
           }
-          float mx[8];
+          float mx[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+          for (int e = 0; e < 4; ++e) mx[e] = fmaxf(sv[2 * e], sv[2 * e + 1]);   // sv[0..7]
 #pragma unroll
-          for (int e = 8; e < 128; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
-          const float tmax =
-              fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-          const float mt = tmax * sl2;
-          const bool need = mt > m_run + kTau;
+          for (int e = 8; e < 128; e += 8) {                                       // sv[8..127]
+            mx[0] = fmax3(mx[0], sv[e], sv[e + 1]);
+            mx[1] = fmax3(mx[1], sv[e + 2], sv[e + 3]);
+            mx[2] = fmax3(mx[2], sv[e + 4], sv[e + 5]);
+            mx[3] = fmax3(mx[3], sv[e + 6], sv[e + 7]);
+          }
+          const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[3]);
+          // running max kept in raw score units: x = (s - m) * c is exactly 0 for the
+          // maximum element, so a lone visible key gets P = 1 exactly
+          const bool need = tmax > m_run + tau_raw;
           float corr = 1.f;
           if (need) {
-            corr = ex2_approx(m_run - mt);
+            corr = ex2_approx((m_run - tmax) * sl2);
             l_run *= corr;
-            m_run = mt;
+            m_run = tmax;
           }
           if (cnt > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -365,20 +380,30 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
           const float mu = (m_run == kNegInf) ? 0.f : m_run;
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          // P = exp2((s - m) * c) two columns at a time: packed subtract and multiply, two
+          // MUFU ex2, one packed add into the running row sum (two independent sum chains)
+          const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mu, -mu);
+          uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2_approx(fmaf(sv[32 * c + 2 * e], sl2, -mu));
-              const float p1 = ex2_approx(fmaf(sv[32 * c + 2 * e + 1], sl2, -mu));
-              ls[e & 3] += p0 + p1;
+              float x0, x1;
+              f2_unpack(f2_mul(f2_add(f2_pack(sv[32 * c + 2 * e], sv[32 * c + 2 * e + 1]), nm2), c2),
+                        x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(p0, p1));
               pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st16(tS + 16 * c, pk);
           }
-          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          {
+            float a0, a1, b0, b1;
+            f2_unpack(acc2[0], a0, a1);
+            f2_unpack(acc2[1], b0, b1);
+            l_run += (a0 + a1) + (b0 + b1);
+          }
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&p_full[q]);
@@ -392,7 +417,8 @@ __global__ void __launch_bounds__(384, 1)
       const long long tok = (a.layout == RA_LAYOUT_STRIPED) ? (long long)loc * a.P + i
                                                           : (long long)i * a.n + loc;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : kNegInf;
+      const float lse_v =
+          l_run > 0.f ? (m_run * sl2 + __log2f(l_run)) * 0.69314718055994531f : kNegInf;
       const size_t row = ((size_t)b * a.L + tok) * a.H + h;
       const size_t lidx = ((size_t)b * a.H + h) * a.L + tok;
       float* of32 = nullptr;
