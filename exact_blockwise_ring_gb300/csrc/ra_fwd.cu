@@ -249,59 +249,76 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      int pend_st[2] = {-1, -1};      // V stage of the item whose PV is still to be issued
-      uint32_t pend_par[2] = {0, 0};
-      int pv_cnt[2] = {0, 0};
+      // per query tile: V stage / phase of the item whose PV is still to be issued (-1:
+      // none) and the number of PVs issued so far; scalars, so nothing goes to local memory
+      int pend0 = -1, pend1 = -1;
+      uint32_t ppar0 = 0, ppar1 = 0;
+      int pv0 = 0, pv1 = 0;
       bool ok = mbar_wait(q_full, 0, wc);
       tc_fence_after();
+      const uint64_t q0d = sdesc_kmajor(q_addr), q1d = sdesc_kmajor(q_addr + C::QB);
+      const uint32_t dS0 = tbase + C::COL_S, dS1 = tbase + C::COL_S + 128;
+      const uint32_t dO0 = tbase + C::COL_O, dO1 = tbase + C::COL_O + D;
 
-      auto issue_pv = [&](int q) -> bool {
-        if (!mbar_wait(&p_full[q], pv_cnt[q] & 1, wc)) return false;
-        if (!mbar_wait(&v_full[pend_st[q]], pend_par[q], wc)) return false;
-        tc_fence_after();
-        const uint32_t vb = v_addr + pend_st[q] * C::KVB;
-        const uint32_t dO = tbase + C::COL_O + q * D;
-        const uint32_t aP = tbase + C::COL_S + q * 128;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(dO, aP + kk * 8, sdesc_mnmajor(vb + kk * 2048, kTile * 128), idPV,
-                  (pv_cnt[q] > 0 || kk > 0) ? 1u : 0u);
-        ++pv_cnt[q];
-        pend_st[q] = -1;
-        return true;
-      };
+#define RA_ISSUE_PV(PEND, PPAR, PV, PFULL, DO_, AP_)                                          \
+  do {                                                                                        \
+    if (!mbar_wait(PFULL, (PV) & 1, wc) || !mbar_wait(&v_full[PEND], PPAR, wc)) {            \
+      ok = false;                                                                             \
+      break;                                                                                  \
+    }                                                                                         \
+    tc_fence_after();                                                                         \
+    const uint64_t vd = sdesc_mnmajor(v_addr + (PEND) * C::KVB, kTile * 128);                 \
+    _Pragma("unroll") for (int kk = 0; kk < kTile / 16; ++kk)                                 \
+        umma_ts(DO_, (AP_) + kk * 8, vd + ((kk * 2048) >> 4), idPV,                           \
+                ((PV) > 0 || kk > 0) ? 1u : 0u);                                              \
+    ++(PV);                                                                                   \
+    (PEND) = -1;                                                                              \
+  } while (0)
+
+#define RA_ISSUE_S(QD, DS_)                                                                   \
+  do {                                                                                        \
+    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                   \
+      const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;                   \
+      umma_ss(DS_, (QD) + off, kd + off, idS, kk > 0 ? 1u : 0u);                              \
+    }                                                                                         \
+  } while (0)
 
       int n = 0;
       for (int k = sc.k0; k < sc.k1 && ok; ++k) {
         const int j = sc.j_of(k);
         const int ue = sc.u_end(j);
-        for (int u = 0; u < ue && ok; ++u, ++n) {
+        for (int u = 0; u < ue; ++u, ++n) {
           const int kst = n % NK, vst = n % NV;
           if (!mbar_wait(&k_full[kst], (n / NK) & 1, wc)) { ok = false; break; }
           tc_fence_after();
-          for (int q = 0; q < 2 && ok; ++q) {
-            if (pend_st[q] >= 0 && !issue_pv(q)) { ok = false; break; }
-            if (sc.cls(q, j, u) != kSkip) {
-              const uint32_t qa = q_addr + q * C::QB, ka = k_addr + kst * C::KVB;
-              const uint32_t dS = tbase + C::COL_S + q * 128;
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-                umma_ss(dS, sdesc_kmajor(qa + off), sdesc_kmajor(ka + off), idS, kk > 0 ? 1u : 0u);
-              }
-              umma_commit(&s_full[q]);
-              pend_st[q] = vst;
-              pend_par[q] = (n / NV) & 1;
-            }
-          }
+          const uint64_t kd = sdesc_kmajor(k_addr + kst * C::KVB);
+          // query tile 0
+          if (pend0 >= 0) RA_ISSUE_PV(pend0, ppar0, pv0, &p_full[0], dO0, dS0);
           if (!ok) break;
+          if (sc.cls(0, j, u) != kSkip) {
+            RA_ISSUE_S(q0d, dS0);
+            umma_commit(&s_full[0]);
+            pend0 = vst;
+            ppar0 = (n / NV) & 1;
+          }
+          // query tile 1
+          if (pend1 >= 0) RA_ISSUE_PV(pend1, ppar1, pv1, &p_full[1], dO1, dS1);
+          if (!ok) break;
+          if (sc.cls(1, j, u) != kSkip) {
+            RA_ISSUE_S(q1d, dS1);
+            umma_commit(&s_full[1]);
+            pend1 = vst;
+            ppar1 = (n / NV) & 1;
+          }
           umma_commit(&k_empty[kst]);                       // both S MMAs of item n issued
           if (n > 0) umma_commit(&v_empty[(n - 1) % NV]);    // every PV of item n-1 issued
         }
       }
-      for (int q = 0; q < 2 && ok; ++q)
-        if (pend_st[q] >= 0 && !issue_pv(q)) ok = false;
+      if (ok && pend0 >= 0) RA_ISSUE_PV(pend0, ppar0, pv0, &p_full[0], dO0, dS0);
+      if (ok && pend1 >= 0) RA_ISSUE_PV(pend1, ppar1, pv1, &p_full[1], dO1, dS1);
       if (ok && n > 0) umma_commit(&v_empty[(n - 1) % NV]);
+#undef RA_ISSUE_PV
+#undef RA_ISSUE_S
       umma_commit(&o_final[0]);
       umma_commit(&o_final[1]);
       umma_commit(drain);
@@ -368,17 +385,6 @@ __global__ void __launch_bounds__(384, 1)
             l_run *= corr;
             m_run = tmax;
           }
-          if (cnt > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tO + 32 * c, r);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-              tmem_st32(tO + 32 * c, r);
-            }
-          }
           const float mu = (m_run == kNegInf) ? 0.f : m_run;
           // P = exp2((s - m) * c) two columns at a time: packed subtract and multiply, two
           // MUFU ex2, one packed add into the running row sum (two independent sum chains)
@@ -403,6 +409,19 @@ __global__ void __launch_bounds__(384, 1)
             f2_unpack(acc2[0], a0, a1);
             f2_unpack(acc2[1], b0, b1);
             l_run += (a0 + a1) + (b0 + b1);
+          }
+          // O *= correction (rare, lazy rescale), after the scores are no longer live; it
+          // must land before P is published, because the next PV accumulates onto O
+          if (cnt > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tO + 32 * c, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+              tmem_st32(tO + 32 * c, r);
+            }
           }
           tmem_wait_st();
           tc_fence_before();
