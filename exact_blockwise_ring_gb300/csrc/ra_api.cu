@@ -368,10 +368,10 @@ ra_status_t ra_bwd_main(const ra_params_t* p, const void* q, const void* k, cons
       !aligned16(dv))
     return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   CUtensorMap tq, tk, tv, tdo;
-  if ((s = make_rows_map(&tq, q, p, 64)) != RA_OK) return s;
+  if ((s = make_rows_map(&tq, q, p, kTile)) != RA_OK) return s;
   if ((s = make_rows_map(&tk, k, p, kTile)) != RA_OK) return s;
   if ((s = make_rows_map(&tv, v, p, kTile)) != RA_OK) return s;
-  if ((s = make_rows_map(&tdo, dout, p, 64)) != RA_OK) return s;
+  if ((s = make_rows_map(&tdo, dout, p, kTile)) != RA_OK) return s;
   BwdArgs a{};
   a.B = p->batch;
   a.H = p->heads;
@@ -458,6 +458,9 @@ ra_status_t ra_check_error(void* workspace, void* stream) {
   if (word != 0) {
     e = cudaMemset(workspace, 0, sizeof(word));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace error word");
+    if (word & 0x10u)
+      return fail(RA_ERR_CUDA, "the backward kernel found its shared-memory base not 1024-byte "
+                  "aligned and did nothing (error word 0x%x)", word);
     return fail(RA_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%x)", word);
   }
   return RA_OK;

@@ -9,26 +9,26 @@
 // order (shard i = (j + k) mod P at step k for KV shard j), so dK and dV accumulate in
 // TMEM and leave once.  dQ partials are added into an fp32 accumulator in global memory.
 //
-// One CTA = 128 keys (tile u of shard j) of one (batch, head).  Query tiles are 64 rows.
-// Roles (512 threads):
-//   warp 0      producer: K, V once (TMA); per query tile Q, dO (TMA) and its 64 lse
+// One CTA = 128 keys (tile u of shard j) of one (batch, head); query tiles of 128 rows.
+// Roles (384 threads):
+//   warp 0      producer: K, V once (TMA); per query tile Q, dO (TMA) and its 128 lse
 //               (log2 domain) and D values (bulk copies from the shard-major arrays the
-//               preprocess kernel wrote)
+//               preprocess kernel wrote), two stages
 //   warp 1      TMEM allocator and tcgen05.mma issuer
 //   warps 4-11  two warpgroups, thread = key row, warpgroup g takes query columns
-//               [32g, 32g+32): P^T = exp2(S^T*c - lse2), dS^T = P^T (dP^T - D), both
-//               rounded to bf16 into 128-byte-swizzled shared tiles; at the end
-//               warpgroup 0 writes dV and warpgroup 1 writes dK
-//   warps 12-15 thread = feature d: dQ^T tile from TMEM -> fp32 reductions into dq_acc
-// MMAs per query tile m (M = 128 rows of TMEM lanes):
-//   S^T  = K Q^T      A K-major smem,    B K-major smem    (N = 64)
-//   dP^T = V dO^T     A K-major,         B K-major         (N = 64)
-//   dV  += P^T dO     A K-major (P^T),   B MN-major (dO)   (N = D)
-//   dK  += dS^T Q     A K-major (dS^T),  B MN-major (Q)    (N = D)
-//   dQ^T = K^T dS^T   A MN-major (K),    B MN-major (dS^T) (N = 64)
-// S^T(m+1) and dP^T(m+1) are issued as soon as the key-row warps have consumed S^T(m),
-// dP^T(m), so their work overlaps dV, dK, dQ of tile m.
-// TMEM columns: S^T [0,64) dP^T [64,128) dQ^T [128,192) dV [256,384) dK [384,512).
+//               [64g, 64g+64): P^T = exp2(S^T*c - lse2) (bf16, back into TMEM as the A
+//               operand of dV) and dS^T = P^T (dP^T - D) (bf16, 128-byte-swizzled shared
+//               tile); then they drain the dQ^T tile (thread = feature row) into the fp32
+//               accumulator; at the end warpgroup 0 writes dV, warpgroup 1 writes dK
+// MMAs per query tile m (M = 128 TMEM lanes, N = 128):
+//   S^T  = K Q^T      A K-major smem,   B K-major smem          -> S region
+//   dP^T = V dO^T     A K-major smem,   B K-major smem          -> dP region
+//   dV  += P^T dO     A TMEM (P^T),     B MN-major smem (dO)
+//   dK  += dS^T Q     A K-major smem,   B MN-major smem (Q)
+//   dQ^T = K^T dS^T   A MN-major smem,  B MN-major smem (dS^T)  -> dP region
+// Issue order once tile m's scores are consumed: dV(m), S^T(m+1), dQ^T(m), [dQ^T drained],
+// dP^T(m+1), dK(m): dK(m) runs while the next tile's scores are being processed.
+// TMEM columns: S^T/P^T [0,128), dP^T/dQ^T [128,256), dV [256,384), dK [384,512).
 #include <cuda_bf16.h>
 
 #include "ra_internal.h"
@@ -38,31 +38,33 @@ namespace ra {
 
 namespace {
 
-constexpr int BQ = 64;      // query rows per tile
+constexpr int BQ = 128;     // query rows per tile
 constexpr int NSTQ = 2;     // query-side pipeline stages
 constexpr int D_ = 128;     // head dim of this kernel
 
 struct BwdCfg {
   static constexpr int KB = kTile * D_ * 2;        // K or V tile bytes (32 KB)
-  static constexpr int QB = BQ * D_ * 2;           // Q or dO tile bytes (16 KB)
-  static constexpr int SB = kTile * BQ * 2;        // P^T or dS^T tile bytes (16 KB)
+  static constexpr int QB = BQ * D_ * 2;           // Q or dO tile bytes (32 KB)
+  static constexpr int SB = kTile * BQ * 2;        // dS^T tile bytes (32 KB)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KB;
   static constexpr int OFF_Q = OFF_V + KB;
   static constexpr int OFF_DO = OFF_Q + NSTQ * QB;
-  static constexpr int OFF_PT = OFF_DO + NSTQ * QB;
-  static constexpr int OFF_DS = OFF_PT + 2 * SB;
-  static constexpr int OFF_LD = OFF_DS + 2 * SB;   // per stage: 64 lse2 + 64 D floats
+  static constexpr int OFF_DS = OFF_DO + NSTQ * QB;
+  static constexpr int OFF_LD = OFF_DS + SB;       // per stage: 128 lse2 + 128 D floats
   static constexpr int LDB = 2 * BQ * 4;
   static constexpr int OFF_BAR = OFF_LD + NSTQ * LDB;
-  // kv_full, q_full[NSTQ], q_empty[NSTQ], s_full, ds_ready, ds_free[2], dq_full, dq_empty,
-  // kv_final, drain
+  // kv_full, q_full[NSTQ], q_empty[NSTQ], s_full, s_read, ds_ready, ds_free, dq_full,
+  // dq_empty, kv_final, drain
   static constexpr int NBAR = 1 + 2 * NSTQ + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
-  static constexpr int COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+  // no alignment slack: the kernel requires (and checks) a 1024-byte aligned base
+  static constexpr int SMEM_BYTES = OFF_MISC + 64;
+  static constexpr int COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
+
+constexpr uint32_t kErrMisaligned = 0x10u;
 
 __device__ __forceinline__ void load_rows(void* dst, const CUtensorMap* m, uint64_t* bar,
                                           int layout, int d0, int h, int shard, int local0,
@@ -99,42 +101,40 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// Query tiles of shard i that see KV tile (j, u): for query tile t (64 rows),
-//   delta = pos offset such that key row b (0..127) is visible to query row a (0..63)
-//           iff a - b + delta >= 0
-//   contiguous: delta = (i - j) * n + 64 t - 128 u
-//   striped:    delta = 64 t - 128 u - (i < j)
-// skip: delta < -63; full: delta >= 127 (or non-causal); otherwise masked.
+// Query tiles of shard i that see KV tile (j, u): for query tile t (128 rows),
+//   key row b (0..127) is visible to query row a (0..127) iff a - b + delta >= 0 with
+//   contiguous: delta = (i - j) * n + 128 (t - u)
+//   striped:    delta = 128 (t - u) - (i < j)
+// skip: delta < -127; full: delta >= 127 (or non-causal); otherwise masked.
 struct BwdSched {
-  int j, u, n, T64, P, layout, causal;
+  int j, u, n, T, P, layout, causal;
   __device__ int i_of(int k) const { return (j + k) % P; }
   __device__ long long delta(int i, int t) const {
-    if (layout == RA_LAYOUT_STRIPED) return 64LL * t - 128LL * u - (i < j ? 1 : 0);
-    return (long long)(i - j) * n + 64LL * t - 128LL * u;
+    if (layout == RA_LAYOUT_STRIPED) return 128LL * (t - u) - (i < j ? 1 : 0);
+    return (long long)(i - j) * n + 128LL * (t - u);
   }
+  // first query tile with delta >= -127
   __device__ int t_lo(int i) const {
     if (!causal) return 0;
-    long long num = (layout == RA_LAYOUT_STRIPED) ? 128LL * u + (i < j ? 1 : 0) - 63
-                                                  : 128LL * u - (long long)(i - j) * n - 63;
+    long long num = (layout == RA_LAYOUT_STRIPED) ? 128LL * u + (i < j ? 1 : 0) - 127
+                                                  : 128LL * u - (long long)(i - j) * n - 127;
     if (num <= 0) return 0;
-    long long t = (num + 63) / 64;
-    return t > T64 ? T64 : (int)t;
+    long long t = (num + 127) / 128;
+    return t > T ? T : (int)t;
   }
 };
 
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(384, 1)
     ra_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs a) {
   using C = BwdCfg;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   uint8_t* sK = sm + C::OFF_K;
   uint8_t* sV = sm + C::OFF_V;
   uint8_t* sQ = sm + C::OFF_Q;
   uint8_t* sDO = sm + C::OFF_DO;
-  uint8_t* sPT = sm + C::OFF_PT;
   uint8_t* sDS = sm + C::OFF_DS;
   float* sLD = reinterpret_cast<float*>(sm + C::OFF_LD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
@@ -142,9 +142,10 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + NSTQ;
   uint64_t* s_full = q_empty + NSTQ;
-  uint64_t* ds_ready = s_full + 1;
+  uint64_t* s_read = s_full + 1;
+  uint64_t* ds_ready = s_read + 1;
   uint64_t* ds_free = ds_ready + 1;
-  uint64_t* dq_full = ds_free + 2;
+  uint64_t* dq_full = ds_free + 1;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* kv_final = dq_empty + 1;
   uint64_t* drain = kv_final + 1;
@@ -155,11 +156,18 @@ __global__ void __launch_bounds__(512, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // The 128-byte swizzle atoms need a 1024-byte aligned base; this kernel carries no
+  // slack to realign, so a misaligned base is reported (error word) instead of used.
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrMisaligned);
+    return;
+  }
+
   // ---- decode: one (batch, head) after another (the resident CTAs then share that
   // head's Q, dO and dQ accumulator in L2); inside a head, heavy KV tiles first --------
   const int per_bh = a.P * a.T;
   const int bh = blockIdx.x / per_bh;
-  int idx = blockIdx.x % per_bh;
+  const int idx = blockIdx.x % per_bh;
   int j, u;
   if (a.layout == RA_LAYOUT_STRIPED || !a.causal) {
     u = idx / a.P;
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(512, 1)
     u = idx % a.T;
   }
   const int b = bh / a.H, h = bh % a.H;
-  const BwdSched sc{j, u, a.n, a.n / BQ, a.P, a.layout, a.causal};
+  const BwdSched sc{j, u, a.n, a.T, a.P, a.layout, a.causal};
 
   if (threadIdx.x == 0) {
     *abort_flag = (*(volatile unsigned int*)a.err != 0u) ? 1u : 0u;
@@ -179,17 +187,17 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&q_empty[st], 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(s_read, 256);
     mbar_init(ds_ready, 256);
-    mbar_init(&ds_free[0], 1);
-    mbar_init(&ds_free[1], 1);
+    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, 256);
     mbar_init(kv_final, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (*abort_flag) return;
+  if (*abort_flag) return;   // an earlier CTA gave up: uniform early exit, nothing held
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -215,7 +223,7 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = true;
       for (int k = 0; k < a.P && ok; ++k) {
         const int i = sc.i_of(k);
-        for (int t = sc.t_lo(i); t < sc.T64; ++t, ++m) {
+        for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
           const int st = m % NSTQ;
           if (m >= NSTQ && !mbar_wait(&q_empty[st], ((m / NSTQ) - 1) & 1, wc)) { ok = false; break; }
           mbar_expect_tx(&q_full[st], 2 * C::QB + C::LDB);
@@ -230,6 +238,7 @@ __global__ void __launch_bounds__(512, 1)
           bulk_load(sLD + st * (2 * BQ) + BQ, a.Dvec + off, BQ * 4, &q_full[st]);
         }
       }
+      // let every copy this thread issued land before the CTA can exit
       mbar_wait_drain(kv_full, 0, a.wait_limit_ns);
       for (int r = (m > NSTQ ? m - NSTQ : 0); r < m; ++r)
         mbar_wait_drain(&q_full[r % NSTQ], (r / NSTQ) & 1, a.wait_limit_ns);
@@ -237,201 +246,233 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp == 1) {
     // ================================================================ MMA issuer ===
     if (lane == 0) {
-      constexpr uint32_t idSP = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
-      constexpr uint32_t idKV = idesc_bf16(128, D_, false, true);    // dV, dK
-      constexpr uint32_t idDQ = idesc_bf16(128, BQ, true, true);     // dQ^T
+      constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t idKM = idesc_bf16(128, D_, false, true);     // dV, dK
+      constexpr uint32_t idMM = idesc_bf16(128, BQ, true, true);      // dQ^T
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
-      const uint32_t pt_addr = smem_u32(sPT), ds_addr = smem_u32(sDS);
-      const uint32_t tS = tbase + C::COL_S, tDP = tbase + C::COL_DP, tDQ = tbase + C::COL_DQ;
+      const uint32_t ds_addr = smem_u32(sDS);
+      const uint32_t tS = tbase + C::COL_S, tDP = tbase + C::COL_DP;
       const uint32_t tDV = tbase + C::COL_DV, tDK = tbase + C::COL_DK;
+      // base descriptors; per-MMA offsets are added in 16-byte units
+      const uint64_t kK = sdesc_kmajor(k_addr), vK = sdesc_kmajor(v_addr);
+      const uint64_t kMN = sdesc_mnmajor(k_addr, kTile * 128);     // K^T: M = features
+      const uint64_t dsK = sdesc_kmajor(ds_addr);                  // dS^T: rows = keys
+      const uint64_t dsMN = sdesc_mnmajor(ds_addr, kTile * 128);   // dS^T: N = queries
       bool ok = mbar_wait(kv_full, 0, wc);
       tc_fence_after();
-      // total query tiles of this CTA
       int total = 0;
-      for (int k = 0; k < a.P; ++k) total += sc.T64 - sc.t_lo(sc.i_of(k));
+      for (int k = 0; k < a.P; ++k) total += sc.T - sc.t_lo(sc.i_of(k));
 
-      auto issue_sdp = [&](int m) -> bool {
-        const int st = m % NSTQ;
-        if (!mbar_wait(&q_full[st], (m / NSTQ) & 1, wc)) return false;
+      // scores: A = K or V (K-major, 128 keys), B = Q or dO tile (K-major), K = D
+#define RA_SCORES(D_TM, AK, BADDR)                                                        \
+  do {                                                                                    \
+    const uint64_t bd_ = sdesc_kmajor(BADDR);                                             \
+    _Pragma("unroll") for (int kk = 0; kk < D_ / 16; ++kk) {                              \
+      const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;               \
+      umma_ss(D_TM, (AK) + off, bd_ + off, idKK, kk > 0 ? 1u : 0u);                       \
+    }                                                                                     \
+  } while (0)
+
+      if (ok && total > 0) {
+        ok = mbar_wait(&q_full[0], 0, wc);
         tc_fence_after();
-        const uint32_t qa = q_addr + st * C::QB, da = do_addr + st * C::QB;
-#pragma unroll
-        for (int kk = 0; kk < D_ / 16; ++kk) {
-          const uint32_t offk = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-          const uint32_t offq = (kk / 4) * (BQ * 128) + (kk % 4) * 32;
-          umma_ss(tS, sdesc_kmajor(k_addr + offk), sdesc_kmajor(qa + offq), idSP, kk > 0);
+        if (ok) {
+          RA_SCORES(tS, kK, q_addr);
+          RA_SCORES(tDP, vK, do_addr);
+          umma_commit(s_full);
         }
-#pragma unroll
-        for (int kk = 0; kk < D_ / 16; ++kk) {
-          const uint32_t offk = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-          const uint32_t offq = (kk / 4) * (BQ * 128) + (kk % 4) * 32;
-          umma_ss(tDP, sdesc_kmajor(v_addr + offk), sdesc_kmajor(da + offq), idSP, kk > 0);
-        }
-        umma_commit(s_full);
-        return true;
-      };
-
-      if (ok && total > 0) ok = issue_sdp(0);
+      }
       for (int m = 0; m < total && ok; ++m) {
-        const int st = m % NSTQ;
+        const int st = m % NSTQ, st1 = (m + 1) % NSTQ;
+        const uint32_t qa = q_addr + st * C::QB, da = do_addr + st * C::QB;
         if (!mbar_wait(ds_ready, m & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        if (m + 1 < total && !issue_sdp(m + 1)) { ok = false; break; }
-        const uint32_t qa = q_addr + st * C::QB, da = do_addr + st * C::QB;
-        const uint32_t pa = pt_addr + (m & 1) * C::SB, dsa = ds_addr + (m & 1) * C::SB;
-        // dV += P^T dO ; dK += dS^T Q   (K = 64 query rows: 4 steps of 16)
+        // dV += P^T dO   (K = 128 query rows; P^T is read from TMEM)
+        {
+          const uint64_t bd = sdesc_mnmajor(da, BQ * 128);
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_ss(tDV, sdesc_kmajor(pa + kk * 32), sdesc_mnmajor(da + kk * 2048, BQ * 128), idKV,
-                  (m > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_ss(tDK, sdesc_kmajor(dsa + kk * 32), sdesc_mnmajor(qa + kk * 2048, BQ * 128), idKV,
-                  (m > 0 || kk > 0) ? 1u : 0u);
-        // dQ^T = K^T dS^T   (K = 128 keys: 8 steps of 16)
-        if (m > 0 && !mbar_wait(dq_empty, (m - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            umma_ts(tDV, tS + kk * 8, bd + ((kk * 2048) >> 4), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+        }
+        // S^T(m+1): the S region is free once dV(m) has read P^T(m) (in-order pipe)
+        if (m + 1 < total) {
+          if (!mbar_wait(&q_full[st1], ((m + 1) / NSTQ) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          RA_SCORES(tS, kK, q_addr + st1 * C::QB);
+        }
+        // dQ^T = K^T dS^T into the dP region (dP^T(m) already consumed)   (K = 128 keys)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tDQ, sdesc_mnmajor(k_addr + kk * 2048, kTile * 128),
-                  sdesc_mnmajor(dsa + kk * 2048, kTile * 128), idDQ, kk > 0 ? 1u : 0u);
+          umma_ss(tDP, kMN + ((kk * 2048) >> 4), dsMN + ((kk * 2048) >> 4), idMM,
+                  kk > 0 ? 1u : 0u);
         umma_commit(dq_full);
-        umma_commit(&q_empty[st]);
-        umma_commit(&ds_free[m & 1]);
+        // dP^T(m+1) once the key-row warps have read dQ^T(m) out of the dP region
+        if (m + 1 < total) {
+          if (!mbar_wait(dq_empty, m & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          RA_SCORES(tDP, vK, do_addr + st1 * C::QB);
+          umma_commit(s_full);
+        }
+        // dK += dS^T Q   (K = 128 query rows); runs under the next tile's score work
+        {
+          const uint64_t bd = sdesc_mnmajor(qa, BQ * 128);
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            const uint32_t offa = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+            umma_ss(tDK, dsK + offa, bd + ((kk * 2048) >> 4), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(ds_free);       // dS^T(m) read by dQ^T(m) and dK(m)
+        umma_commit(&q_empty[st]);  // Q(m), dO(m) read for the last time
       }
+#undef RA_SCORES
       umma_commit(kv_final);
       umma_commit(drain);
       if (!ok) mbar_wait_drain(drain, 0, a.wait_limit_ns);
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4) {
     // ================================================================ key rows =====
     const int wq = warp & 3;
-    const int half = (warp - 4) >> 2;             // query columns [32*half, 32*half + 32)
-    const int brow = wq * 32 + lane;              // key row in the tile
+    const int half = (warp - 4) >> 2;             // query columns [64*half, 64*half + 64)
+    const int brow = wq * 32 + lane;              // key row (and, for dQ^T, feature row)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tbase + lane_off + C::COL_S + 32 * half;
-    const uint32_t tDP = tbase + lane_off + C::COL_DP + 32 * half;
+    const uint32_t tS = tbase + lane_off + C::COL_S + 64 * half;
+    const uint32_t tDP = tbase + lane_off + C::COL_DP + 64 * half;
+    const uint32_t tP = tbase + lane_off + C::COL_S + 32 * half;    // P^T bf16 pairs
     const float sl2 = a.scale_log2;
+    float* dq_head = a.dq_acc + (size_t)b * a.L * a.H * D_ + (size_t)h * D_ + brow;
+    const long long qstride = (a.layout == RA_LAYOUT_STRIPED) ? (long long)a.P * a.H * D_
+                                                              : (long long)a.H * D_;
     bool ok = true;
     int m = 0;
     for (int k = 0; k < a.P && ok; ++k) {
       const int i = sc.i_of(k);
-      for (int t = sc.t_lo(i); t < sc.T64; ++t, ++m) {
+      for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
         const int st = m % NSTQ;
         if (!mbar_wait(s_full, m & 1, wc) || !mbar_wait(&q_full[st], (m / NSTQ) & 1, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t sr[32], pr[32];
-        tmem_ld32(tS, sr);
-        tmem_ld32(tDP, pr);
-        tmem_wait_ld();
-        const float* lse2 = sLD + st * (2 * BQ) + 32 * half;
-        const float* dv = lse2 + BQ;
-        const long long dl = a.causal ? sc.delta(i, t) : 1000000LL;
-        // visible iff col - brow + delta >= 0  ->  col >= brow - delta (col = 32*half + c)
-        const long long lim = (long long)brow - dl - 32 * half;
-        if (m >= 2 && !mbar_wait(&ds_free[m & 1], ((m >> 1) - 1) & 1, wc)) { ok = false; break; }
-        uint8_t* prow = sPT + (m & 1) * C::SB + brow * 128;
-        uint8_t* drow = sDS + (m & 1) * C::SB + brow * 128;
+        uint32_t sr[64], pr[64];
+        {
+          uint32_t r[32];
+          tmem_ld32(tS, r);
 #pragma unroll
-        for (int c8l = 0; c8l < 4; ++c8l) {
-          const int c8 = 4 * half + c8l;
-          // the 8 columns' lse2 and D: two 16-byte broadcast loads each
+          for (int e = 0; e < 32; ++e) sr[e] = r[e];
+          tmem_ld32(tS + 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sr[32 + e] = r[e];
+          tmem_ld32(tDP, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pr[e] = r[e];
+          tmem_ld32(tDP + 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pr[32 + e] = r[e];
+          tmem_wait_ld();
+        }
+        // both warpgroups have read their S^T columns before P^T overwrites [0, 64)
+        tc_fence_before();
+        mbar_arrive(s_read);
+        if (!mbar_wait(s_read, m & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const float* lse2 = sLD + st * (2 * BQ) + 64 * half;
+        const float* dvec = lse2 + BQ;
+        const long long dl = a.causal ? sc.delta(i, t) : (1LL << 40);
+        // visible iff col - brow + delta >= 0 with col = 64*half + c, i.e. c >= lim
+        const long long lim = (long long)brow - dl - 64 * half;
+        uint32_t pw[32], dw[32];
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
           float lv[8], dd[8];
-          *reinterpret_cast<float4*>(&lv[0]) = reinterpret_cast<const float4*>(lse2)[2 * c8l];
-          *reinterpret_cast<float4*>(&lv[4]) = reinterpret_cast<const float4*>(lse2)[2 * c8l + 1];
-          *reinterpret_cast<float4*>(&dd[0]) = reinterpret_cast<const float4*>(dv)[2 * c8l];
-          *reinterpret_cast<float4*>(&dd[4]) = reinterpret_cast<const float4*>(dv)[2 * c8l + 1];
-          uint32_t pw[4], dw[4];
+          *reinterpret_cast<float4*>(&lv[0]) = reinterpret_cast<const float4*>(lse2)[2 * c8];
+          *reinterpret_cast<float4*>(&lv[4]) = reinterpret_cast<const float4*>(lse2)[2 * c8 + 1];
+          *reinterpret_cast<float4*>(&dd[0]) = reinterpret_cast<const float4*>(dvec)[2 * c8];
+          *reinterpret_cast<float4*>(&dd[4]) = reinterpret_cast<const float4*>(dvec)[2 * c8 + 1];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
             float p[2], ds[2];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const int cl = e2 * 2 + h2;
-              const int c = c8l * 8 + cl;
-              const float s = __uint_as_float(sr[c]);
-              float pv = ex2_approx(fmaf(s, sl2, -lv[cl]));
+              const int c = c8 * 8 + cl;
+              float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[cl]));
               if ((long long)c < lim) pv = 0.f;
               p[h2] = pv;
               ds[h2] = pv * (__uint_as_float(pr[c]) - dd[cl]);
             }
-            pw[e2] = pack_bf16x2(p[0], p[1]);
-            dw[e2] = pack_bf16x2(ds[0], ds[1]);
+            pw[c8 * 4 + e2] = pack_bf16x2(p[0], p[1]);
+            dw[c8 * 4 + e2] = pack_bf16x2(ds[0], ds[1]);
           }
-          const int phys = (c8 ^ (brow & 7)) * 16;
-          *reinterpret_cast<uint4*>(prow + phys) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-          *reinterpret_cast<uint4*>(drow + phys) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
         }
+        // P^T -> TMEM (A operand of dV): columns [32*half, 32*half + 32)
+        {
+          uint32_t v0[16], v1[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            v0[e] = pw[e];
+            v1[e] = pw[16 + e];
+          }
+          tmem_st16(tP, v0);
+          tmem_st16(tP + 16, v1);
+        }
+        // dS^T -> shared: column block `half` of the [128 keys x 128 queries] tile, once
+        // dQ^T(m-1) and dK(m-1) are done reading it
+        if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) { ok = false; break; }
+        uint8_t* drow = sDS + half * (kTile * 128) + brow * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          *reinterpret_cast<uint4*>(drow + ((c8 ^ (brow & 7)) * 16)) =
+              make_uint4(dw[4 * c8], dw[4 * c8 + 1], dw[4 * c8 + 2], dw[4 * c8 + 3]);
         fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(ds_ready);
+        // ---- drain dQ^T(m): thread = feature row brow, query columns [64h, 64h+64) ----
+        if (!mbar_wait(dq_full, m & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t q0[32], q1[32];
+        tmem_ld32(tDP, q0);
+        tmem_ld32(tDP + 32, q1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        const long long tok0 = (a.layout == RA_LAYOUT_STRIPED)
+                                   ? (long long)(t * BQ + 64 * half) * a.P + i
+                                   : (long long)i * a.n + t * BQ + 64 * half;
+        float* p0 = dq_head + tok0 * a.H * D_;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * qstride, __uint_as_float(q0[c]));
+#pragma unroll
+        for (int c = 0; c < 32; ++c) red_add_f32(p0 + (32 + c) * qstride, __uint_as_float(q1[c]));
       }
     }
-    // ---- dK, dV epilogue (thread = key row) ----------------------------------------
+    // ---- dK, dV epilogue (thread = key row): warpgroup 0 writes dV, 1 writes dK ------
     if (ok && mbar_wait(kv_final, 0, wc)) {
       tc_fence_after();
       const int loc = u * kTile + brow;
       const long long tok = (a.layout == RA_LAYOUT_STRIPED) ? (long long)loc * a.P + j
                                                           : (long long)j * a.n + loc;
       const size_t row = ((size_t)b * a.L + tok) * a.H + h;
-      __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(a.dv) + row * D_;
-      __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(a.dk) + row * D_;
       const bool any = m > 0;
-      {
-        const int which = half;
-        const uint32_t tcol = tbase + lane_off + (which ? C::COL_DK : C::COL_DV);
-        const float mul = which ? a.scale : 1.f;
-        __nv_bfloat16* dst = which ? dkp : dvp;
+      const uint32_t tcol = tbase + lane_off + (half ? C::COL_DK : C::COL_DV);
+      const float mul = half ? a.scale : 1.f;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(half ? a.dk : a.dv) + row * D_;
 #pragma unroll
-        for (int c = 0; c < D_ / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tcol + 32 * c, r);
-          tmem_wait_ld();
-          uint4* o = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float f[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) f[x] = any ? __uint_as_float(r[8 * e + x]) * mul : 0.f;
-            o[e] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                              pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-          }
-        }
-      }
-    }
-  } else if (warp >= 12) {
-    // ================================================================ dQ drain =====
-    const int wq = warp & 3;
-    const int d = wq * 32 + lane;                 // feature owned by this thread
-    const uint32_t tDQ = tbase + (static_cast<uint32_t>(wq * 32) << 16) + C::COL_DQ;
-    bool ok = true;
-    int m = 0;
-    for (int k = 0; k < a.P && ok; ++k) {
-      const int i = sc.i_of(k);
-      for (int t = sc.t_lo(i); t < sc.T64; ++t, ++m) {
-        if (!mbar_wait(dq_full, m & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tDQ, r0);
-        tmem_ld32(tDQ + 32, r1);
+      for (int c = 0; c < D_ / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tcol + 32 * c, r);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        // query rows t*64 + c of shard i
-        float* base = a.dq_acc + (size_t)b * a.L * a.H * D_ + (size_t)h * D_ + d;
-        const long long stride = (a.layout == RA_LAYOUT_STRIPED) ? (long long)a.P * a.H * D_
-                                                                 : (long long)a.H * D_;
-        const long long tok0 = (a.layout == RA_LAYOUT_STRIPED) ? (long long)t * BQ * a.P + i
-                                                               : (long long)i * a.n + t * BQ;
-        float* p0 = base + tok0 * a.H * D_;
+        uint4* o = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * stride, __uint_as_float(r0[c]));
+        for (int e = 0; e < 4; ++e) {
+          float f[8];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) red_add_f32(p0 + (32 + c) * stride, __uint_as_float(r1[c]));
+          for (int x = 0; x < 8; ++x) f[x] = any ? __uint_as_float(r[8 * e + x]) * mul : 0.f;
+          o[e] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                            pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        }
       }
     }
   }
@@ -454,7 +495,7 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMa
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.B * a.H * a.P * a.T;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ra_bwd_kernel<<<(unsigned)grid, 512, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  ra_bwd_kernel<<<(unsigned)grid, 384, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
