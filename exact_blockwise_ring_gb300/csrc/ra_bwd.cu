@@ -10,24 +10,27 @@
 // TMEM and leave once.  dQ partials are added into an fp32 accumulator in global memory.
 //
 // One CTA = 128 keys (tile u of shard j) of one (batch, head); query tiles of 128 rows.
-// Roles (384 threads):
+// Roles (640 threads):
 //   warp 0      producer: K, V once (TMA); per query tile Q, dO (TMA) and its 128 lse
 //               (log2 domain) and D values (bulk copies from the shard-major arrays the
 //               preprocess kernel wrote), two stages
 //   warp 1      TMEM allocator and tcgen05.mma issuer
 //   warps 4-11  two warpgroups, thread = key row, warpgroup g takes query columns
-//               [64g, 64g+64): P^T = exp2(S^T*c - lse2) (bf16, back into TMEM as the A
-//               operand of dV) and dS^T = P^T (dP^T - D) (bf16, 128-byte-swizzled shared
-//               tile); then they drain the dQ^T tile (thread = feature row) into the fp32
-//               accumulator; at the end warpgroup 0 writes dV, warpgroup 1 writes dK
+//               [64g, 64g+64) in four passes of 16: P^T = exp2(S^T*c - lse2) (bf16, back
+//               into TMEM inside its own S^T columns, as the A operand of dV) and
+//               dS^T = P^T (dP^T - D) (bf16, 128-byte-swizzled shared tile); at the end
+//               warpgroup 0 writes dV, warpgroup 1 writes dK
+//   warps 12-19 two warpgroups draining dQ^T (thread = feature row, 64 query columns
+//               each) into the fp32 accumulator with coalesced reductions, which then run
+//               in the background of the next tiles' work
 // MMAs per query tile m (M = 128 TMEM lanes, N = 128):
 //   S^T  = K Q^T      A K-major smem,   B K-major smem          -> S region
 //   dP^T = V dO^T     A K-major smem,   B K-major smem          -> dP region
 //   dV  += P^T dO     A TMEM (P^T),     B MN-major smem (dO)
 //   dK  += dS^T Q     A K-major smem,   B MN-major smem (Q)
 //   dQ^T = K^T dS^T   A MN-major smem,  B MN-major smem (dS^T)  -> dP region
-// Issue order once tile m's scores are consumed: dV(m), S^T(m+1), dQ^T(m), [dQ^T drained],
-// dP^T(m+1), dK(m): dK(m) runs while the next tile's scores are being processed.
+// Issue order once tile m's scores are consumed: dQ^T(m), dV(m), S^T(m+1), [dQ^T drained],
+// dP^T(m+1), dK(m): the drain overlaps dV and S^T, dK(m) overlaps the next tile's scores.
 // TMEM columns: S^T/P^T [0,128), dP^T/dQ^T [128,256), dV [256,384), dK [384,512).
 #include <cuda_bf16.h>
 
@@ -54,9 +57,9 @@ struct BwdCfg {
   static constexpr int OFF_LD = OFF_DS + SB;       // per stage: 128 lse2 + 128 D floats
   static constexpr int LDB = 2 * BQ * 4;
   static constexpr int OFF_BAR = OFF_LD + NSTQ * LDB;
-  // kv_full, q_full[NSTQ], q_empty[NSTQ], s_full, s_read, ds_ready, ds_free, dq_full,
-  // dq_empty, kv_final, drain
-  static constexpr int NBAR = 1 + 2 * NSTQ + 8;
+  // kv_full, q_full[NSTQ], q_empty[NSTQ], s_full, ds_ready, ds_free, dq_full, dq_empty,
+  // kv_final, drain
+  static constexpr int NBAR = 1 + 2 * NSTQ + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // no alignment slack: the kernel requires (and checks) a 1024-byte aligned base
   static constexpr int SMEM_BYTES = OFF_MISC + 64;
@@ -124,7 +127,7 @@ struct BwdSched {
   }
 };
 
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(640, 1)
     ra_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs a) {
@@ -142,8 +145,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + NSTQ;
   uint64_t* s_full = q_empty + NSTQ;
-  uint64_t* s_read = s_full + 1;
-  uint64_t* ds_ready = s_read + 1;
+  uint64_t* ds_ready = s_full + 1;
   uint64_t* ds_free = ds_ready + 1;
   uint64_t* dq_full = ds_free + 1;
   uint64_t* dq_empty = dq_full + 1;
@@ -187,7 +189,6 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&q_empty[st], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_read, 256);
     mbar_init(ds_ready, 256);
     mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
@@ -288,27 +289,28 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t qa = q_addr + st * C::QB, da = do_addr + st * C::QB;
         if (!mbar_wait(ds_ready, m & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        // dV += P^T dO   (K = 128 query rows; P^T is read from TMEM)
-        {
-          const uint64_t bd = sdesc_mnmajor(da, BQ * 128);
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            umma_ts(tDV, tS + kk * 8, bd + ((kk * 2048) >> 4), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        }
-        // S^T(m+1): the S region is free once dV(m) has read P^T(m) (in-order pipe)
-        if (m + 1 < total) {
-          if (!mbar_wait(&q_full[st1], ((m + 1) / NSTQ) & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          RA_SCORES(tS, kK, q_addr + st1 * C::QB);
-        }
-        // dQ^T = K^T dS^T into the dP region (dP^T(m) already consumed)   (K = 128 keys)
+        // dQ^T = K^T dS^T into the dP region (dP^T(m) already consumed)   (K = 128 keys);
+        // first, so that the drain warps can start on it while dV and S^T(m+1) run
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ss(tDP, kMN + ((kk * 2048) >> 4), dsMN + ((kk * 2048) >> 4), idMM,
                   kk > 0 ? 1u : 0u);
         umma_commit(dq_full);
-        // dP^T(m+1) once the key-row warps have read dQ^T(m) out of the dP region
+        // dV += P^T dO   (K = 128 query rows; P^T is read from TMEM: warpgroup g left the
+        // bf16 pairs of query columns [64g, 64g+64) in TMEM columns [64g, 64g+32))
+        {
+          const uint64_t bd = sdesc_mnmajor(da, BQ * 128);
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            umma_ts(tDV, tS + (kk / 4) * 64 + (kk % 4) * 8, bd + ((kk * 2048) >> 4), idKM,
+                    (m > 0 || kk > 0) ? 1u : 0u);
+        }
         if (m + 1 < total) {
+          // S^T(m+1): the S region is free once dV(m) has read P^T(m) (in-order pipe)
+          if (!mbar_wait(&q_full[st1], ((m + 1) / NSTQ) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          RA_SCORES(tS, kK, q_addr + st1 * C::QB);
+          // dP^T(m+1) once the drain warps have read dQ^T(m) out of the dP region
           if (!mbar_wait(dq_empty, m & 1, wc)) { ok = false; break; }
           tc_fence_after();
           RA_SCORES(tDP, vK, do_addr + st1 * C::QB);
@@ -331,19 +333,16 @@ __global__ void __launch_bounds__(384, 1)
       umma_commit(drain);
       if (!ok) mbar_wait_drain(drain, 0, a.wait_limit_ns);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ================================================================ key rows =====
     const int wq = warp & 3;
     const int half = (warp - 4) >> 2;             // query columns [64*half, 64*half + 64)
-    const int brow = wq * 32 + lane;              // key row (and, for dQ^T, feature row)
+    const int brow = wq * 32 + lane;              // key row
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tbase + lane_off + C::COL_S + 64 * half;
     const uint32_t tDP = tbase + lane_off + C::COL_DP + 64 * half;
-    const uint32_t tP = tbase + lane_off + C::COL_S + 32 * half;    // P^T bf16 pairs
     const float sl2 = a.scale_log2;
-    float* dq_head = a.dq_acc + (size_t)b * a.L * a.H * D_ + (size_t)h * D_ + brow;
-    const long long qstride = (a.layout == RA_LAYOUT_STRIPED) ? (long long)a.P * a.H * D_
-                                                              : (long long)a.H * D_;
+    uint8_t* drow = sDS + half * (kTile * 128) + brow * 128;
     bool ok = true;
     int m = 0;
     for (int k = 0; k < a.P && ok; ++k) {
@@ -354,98 +353,59 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        tc_fence_after();
-        uint32_t sr[64], pr[64];
-        {
-          uint32_t r[32];
-          tmem_ld32(tS, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sr[e] = r[e];
-          tmem_ld32(tS + 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sr[32 + e] = r[e];
-          tmem_ld32(tDP, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[e] = r[e];
-          tmem_ld32(tDP + 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[32 + e] = r[e];
-          tmem_wait_ld();
-        }
-        // both warpgroups have read their S^T columns before P^T overwrites [0, 64)
-        tc_fence_before();
-        mbar_arrive(s_read);
-        if (!mbar_wait(s_read, m & 1, wc)) { ok = false; break; }
+        // dS^T(m) overwrites the shared tile once dQ^T(m-1) and dK(m-1) have read it
+        if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         const float* lse2 = sLD + st * (2 * BQ) + 64 * half;
         const float* dvec = lse2 + BQ;
         const long long dl = a.causal ? sc.delta(i, t) : (1LL << 40);
         // visible iff col - brow + delta >= 0 with col = 64*half + c, i.e. c >= lim
         const long long lim = (long long)brow - dl - 64 * half;
-        uint32_t pw[32], dw[32];
+        // four passes of 16 query columns; pass p writes its P^T pairs to TMEM columns
+        // [64*half + 8p, +8), inside S^T columns this warpgroup has already read
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float lv[8], dd[8];
-          *reinterpret_cast<float4*>(&lv[0]) = reinterpret_cast<const float4*>(lse2)[2 * c8];
-          *reinterpret_cast<float4*>(&lv[4]) = reinterpret_cast<const float4*>(lse2)[2 * c8 + 1];
-          *reinterpret_cast<float4*>(&dd[0]) = reinterpret_cast<const float4*>(dvec)[2 * c8];
-          *reinterpret_cast<float4*>(&dd[4]) = reinterpret_cast<const float4*>(dvec)[2 * c8 + 1];
+        for (int pass = 0; pass < 4; ++pass) {
+          uint32_t sr[16], pr[16];
+          tmem_ld16(tS + 16 * pass, sr);
+          tmem_ld16(tDP + 16 * pass, pr);
+          tmem_wait_ld();
+          uint32_t pw[8], dw[8];
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            float p[2], ds[2];
+          for (int g8 = 0; g8 < 2; ++g8) {
+            const int cb = 16 * pass + 8 * g8;      // first of 8 columns
+            float lv[8], dd[8];
+            *reinterpret_cast<float4*>(&lv[0]) = *reinterpret_cast<const float4*>(lse2 + cb);
+            *reinterpret_cast<float4*>(&lv[4]) = *reinterpret_cast<const float4*>(lse2 + cb + 4);
+            *reinterpret_cast<float4*>(&dd[0]) = *reinterpret_cast<const float4*>(dvec + cb);
+            *reinterpret_cast<float4*>(&dd[4]) = *reinterpret_cast<const float4*>(dvec + cb + 4);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int cl = e2 * 2 + h2;
-              const int c = c8 * 8 + cl;
-              float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[cl]));
-              if ((long long)c < lim) pv = 0.f;
-              p[h2] = pv;
-              ds[h2] = pv * (__uint_as_float(pr[c]) - dd[cl]);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              float pp[2], ds[2];
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int cl = 2 * e2 + h2;
+                const int c = cb + cl;
+                float pv = ex2_approx(fmaf(__uint_as_float(sr[8 * g8 + cl]), sl2, -lv[cl]));
+                if ((long long)c < lim) pv = 0.f;
+                pp[h2] = pv;
+                ds[h2] = pv * (__uint_as_float(pr[8 * g8 + cl]) - dd[cl]);
+              }
+              pw[4 * g8 + e2] = pack_bf16x2(pp[0], pp[1]);
+              dw[4 * g8 + e2] = pack_bf16x2(ds[0], ds[1]);
             }
-            pw[c8 * 4 + e2] = pack_bf16x2(p[0], p[1]);
-            dw[c8 * 4 + e2] = pack_bf16x2(ds[0], ds[1]);
+          }
+          tmem_st8(tbase + lane_off + C::COL_S + 64 * half + 8 * pass, pw);
+#pragma unroll
+          for (int g8 = 0; g8 < 2; ++g8) {
+            const int c8 = 2 * pass + g8;           // 16-byte chunk inside the 128-byte row
+            *reinterpret_cast<uint4*>(drow + ((c8 ^ (brow & 7)) * 16)) =
+                make_uint4(dw[4 * g8], dw[4 * g8 + 1], dw[4 * g8 + 2], dw[4 * g8 + 3]);
           }
         }
-        // P^T -> TMEM (A operand of dV): columns [32*half, 32*half + 32)
-        {
-          uint32_t v0[16], v1[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            v0[e] = pw[e];
-            v1[e] = pw[16 + e];
-          }
-          tmem_st16(tP, v0);
-          tmem_st16(tP + 16, v1);
-        }
-        // dS^T -> shared: column block `half` of the [128 keys x 128 queries] tile, once
-        // dQ^T(m-1) and dK(m-1) are done reading it
-        if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) { ok = false; break; }
-        uint8_t* drow = sDS + half * (kTile * 128) + brow * 128;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4*>(drow + ((c8 ^ (brow & 7)) * 16)) =
-              make_uint4(dw[4 * c8], dw[4 * c8 + 1], dw[4 * c8 + 2], dw[4 * c8 + 3]);
         fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(ds_ready);
-        // ---- drain dQ^T(m): thread = feature row brow, query columns [64h, 64h+64) ----
-        if (!mbar_wait(dq_full, m & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t q0[32], q1[32];
-        tmem_ld32(tDP, q0);
-        tmem_ld32(tDP + 32, q1);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        const long long tok0 = (a.layout == RA_LAYOUT_STRIPED)
-                                   ? (long long)(t * BQ + 64 * half) * a.P + i
-                                   : (long long)i * a.n + t * BQ + 64 * half;
-        float* p0 = dq_head + tok0 * a.H * D_;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * qstride, __uint_as_float(q0[c]));
-#pragma unroll
-        for (int c = 0; c < 32; ++c) red_add_f32(p0 + (32 + c) * qstride, __uint_as_float(q1[c]));
       }
     }
     // ---- dK, dV epilogue (thread = key row): warpgroup 0 writes dV, 1 writes dK ------
@@ -475,6 +435,39 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
+  } else if (warp >= 12) {
+    // ================================================================ dQ drain =====
+    // thread = feature row d (TMEM lane), warpgroup g takes query columns [64g, 64g+64)
+    const int wq = warp & 3;
+    const int half = (warp - 12) >> 2;
+    const int drow = wq * 32 + lane;
+    const uint32_t tQ = tbase + (static_cast<uint32_t>(wq * 32) << 16) + C::COL_DP + 64 * half;
+    float* dq_head = a.dq_acc + (size_t)b * a.L * a.H * D_ + (size_t)h * D_ + drow;
+    const long long qstride = (a.layout == RA_LAYOUT_STRIPED) ? (long long)a.P * a.H * D_
+                                                              : (long long)a.H * D_;
+    bool ok = true;
+    int m = 0;
+    for (int k = 0; k < a.P && ok; ++k) {
+      const int i = sc.i_of(k);
+      for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
+        if (!mbar_wait(dq_full, m & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t q0[32], q1[32];
+        tmem_ld32(tQ, q0);
+        tmem_ld32(tQ + 32, q1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        const long long tok0 = (a.layout == RA_LAYOUT_STRIPED)
+                                   ? (long long)(t * BQ + 64 * half) * a.P + i
+                                   : (long long)i * a.n + t * BQ + 64 * half;
+        float* p0 = dq_head + tok0 * a.H * D_;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * qstride, __uint_as_float(q0[c]));
+#pragma unroll
+        for (int c = 0; c < 32; ++c) red_add_f32(p0 + (32 + c) * qstride, __uint_as_float(q1[c]));
+      }
+    }
   }
 
   tc_fence_before();
@@ -495,7 +488,7 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMa
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.B * a.H * a.P * a.T;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ra_bwd_kernel<<<(unsigned)grid, 384, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  ra_bwd_kernel<<<(unsigned)grid, 640, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
