@@ -1,0 +1,73 @@
+"""GPU parity at the full workload sizes (32k, 262k, 1M tokens), in the launch
+configuration the benchmark times.
+
+The oracle cannot run these problems whole, so it checks what it can compute one row at a
+time: sampled output rows and lse (O(L*D) each), sampled dQ rows, and, for dK and dV,
+identities that hold at any size: the rows of dS sum to zero, so the sum over keys of dK
+vanishes, and the rows of P sum to one, so the sum over keys of dV equals the sum over
+queries of dO.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_blockwise_ring_gb300 as era
+from exact_blockwise_ring_gb300.synthetic import WORKLOADS, SEEDS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL, LSE_TOL, GRAD_TOL = 1e-2, 1e-3, 2e-2
+
+
+def _rows(L, P, layout):
+    """Sampled query rows: both ends, shard boundaries and a few interior rows."""
+    n = L // P
+    picks = {0, 1, L - 1, n - 1, n, L // 2, L // 3 + 7, 5 * L // 7 + 3}
+    return sorted(r for r in picks if 0 <= r < L)
+
+
+CASES = [("32k", "striped"), ("262k", "striped"), ("1m", "striped"), ("1m", "contiguous")]
+
+
+@pytest.mark.parametrize("name,layout", CASES)
+def test_fullsize_parity(name, layout):
+    w = WORKLOADS[name]
+    B, L, H, D, P, blk = (w["batch"], w["seq_len"], w["heads"], w["head_dim"], w["P"],
+                          w["block"])
+    dev = torch.device("cuda:0")
+    q, k, v, do = make_inputs(B, L, H, D, SEEDS[name], device=dev)
+    out, lse = era.ra_fwd(q, k, v, P, blk, layout, True)               # as the bench runs it
+    dq, dk, dv = era.ra_bwd(q, k, v, out, lse, do, P, blk, layout, True)
+    o32, l32 = era.ra_fwd(q, k, v, P, blk, layout, True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+
+    rows = _rows(L, P, layout)
+    for h in sorted({0, H - 1}):
+        # one head on the host in float64 (only its keys/values are needed)
+        qh, kh, vh, doh = (t[0, :, h, :].double().cpu().numpy()[None, :, None, :]
+                           for t in (q, k, v, do))
+        ro, rl = oracle.attention_rows_fwd(qh, kh, vh, 0, 0, rows, causal=True)
+        go = o32[0, rows, h, :].double().cpu().numpy()
+        gl = l32[0, h, rows].double().cpu().numpy()
+        assert np.max(np.abs(go - ro)) <= OUT_TOL
+        assert np.max(np.abs(gl - rl)) <= LSE_TOL
+        gb = out[0, rows, h, :].double().cpu().numpy()
+        assert np.all(np.abs(gb - ro) <= OUT_TOL + 2.0 ** -8 * np.abs(ro))
+        # dQ: the tolerance is a relative Frobenius error over the whole tensor, estimated
+        # on a seeded uniform sample of rows (boundary rows would over-weight the few
+        # first rows, whose dS = P (dP - D) nearly cancels and so carries the bf16
+        # rounding of O inside D)
+        qrows = np.sort(np.random.default_rng(17 + h).choice(L, size=24, replace=False))
+        rq = oracle.attention_rows_dq(qh, kh, vh, doh, 0, 0, qrows, causal=True)
+        gq = dq[0, qrows, h, :].double().cpu().numpy()
+        assert np.linalg.norm(gq - rq) / np.linalg.norm(rq) <= GRAD_TOL
+
+    # identities over all keys of every head (float64 sums on the device)
+    sk = dk.double().sum(dim=1)
+    assert float(sk.norm() / dk.double().norm()) <= GRAD_TOL
+    sv = dv.double().sum(dim=1)
+    so = do.double().sum(dim=1)
+    assert float((sv - so).norm() / so.norm()) <= GRAD_TOL
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
