@@ -208,17 +208,17 @@ def source_hash(*names):
 
 
 def traffic_for(kernel, src_files):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source has
-    not changed since it was captured; else None."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    """DRAM bytes per launch from the committed ncu summary (profiles/ncu_traffic.txt), if
+    the kernel source has not changed since it was captured; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    e = d.get(kernel)
-    if not e or e.get("source_hash") != source_hash(*src_files):
-        return None
-    return e.get("bytes_per_launch_scaled", e.get("bytes_per_launch"))
+        for ln in f:
+            fl = ln.split()
+            if len(fl) >= 5 and not ln.startswith("#") and fl[0] == kernel:
+                return int(fl[1]) if fl[4] == source_hash(*src_files) else None
+    return None
 
 
 # ---------------------------------------------------------------- our arm ----------
