@@ -72,9 +72,10 @@ __global__ void __launch_bounds__(256)
 }
 
 // Backward preprocess, one warp per row (b, token, h):
-//   D[b, h, shard, local]    = sum_d dO[b, token, h, d] * O[b, token, h, d]
-//   lse2[b, h, shard, local] = lse[b, h, token] * log2(e)
-// written shard-major so the 64 values of one query tile are one contiguous block.
+//   nD[b, h, shard, local]    = -sum_d dO[b, token, h, d] * O[b, token, h, d]
+//   nlse2[b, h, shard, local] = -lse[b, h, token] * log2(e)
+// written shard-major so the values of one query tile are one contiguous block, and
+// negated so that the backward's s*c - lse2 and dP - D are single packed FMAs/adds.
 __global__ void __launch_bounds__(256)
     bwd_pre_kernel(const void* __restrict__ out, int out_fp32, const __nv_bfloat16* __restrict__ dout,
                    const float* __restrict__ lse, float* __restrict__ Dsm, float* __restrict__ L2sm,
@@ -114,8 +115,8 @@ __global__ void __launch_bounds__(256)
     const long long local = (layout == RA_LAYOUT_STRIPED) ? tok / P : tok % n;
     const size_t bh = (size_t)b * H + h;
     const size_t dst = (bh * P + shard) * n + local;
-    Dsm[dst] = acc;
-    L2sm[dst] = lse[bh * L + tok] * 1.4426950408889634f;
+    Dsm[dst] = -acc;
+    L2sm[dst] = -lse[bh * L + tok] * 1.4426950408889634f;
   }
 }
 

@@ -356,13 +356,17 @@ __global__ void __launch_bounds__(640, 1)
         // dS^T(m) overwrites the shared tile once dQ^T(m-1) and dK(m-1) have read it
         if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        const float* lse2 = sLD + st * (2 * BQ) + 64 * half;
-        const float* dvec = lse2 + BQ;
+        const float* lse2 = sLD + st * (2 * BQ) + 64 * half;   // -lse * log2(e)
+        const float* dvec = lse2 + BQ;                          // -D
         const long long dl = a.causal ? sc.delta(i, t) : (1LL << 40);
         // visible iff col - brow + delta >= 0 with col = 64*half + c, i.e. c >= lim
         const long long lim = (long long)brow - dl - 64 * half;
         // four passes of 16 query columns; pass p writes its P^T pairs to TMEM columns
-        // [64*half + 8p, +8), inside S^T columns this warpgroup has already read
+        // [64*half + 8p, +8), inside S^T columns this warpgroup has already read.
+        // Column pairs go through the packed fp32x2 FMA pipe: x = s*c + (-lse2),
+        // dS = P * (dP + (-D)); the mask is applied only on tiles that need one.
+        const bool masked = __any_sync(0xffffffffu, lim > 0);   // whole warp votes
+        const uint64_t c2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int pass = 0; pass < 4; ++pass) {
           uint32_t sr[16], pr[16];
@@ -373,25 +377,32 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
           for (int g8 = 0; g8 < 2; ++g8) {
             const int cb = 16 * pass + 8 * g8;      // first of 8 columns
-            float lv[8], dd[8];
-            *reinterpret_cast<float4*>(&lv[0]) = *reinterpret_cast<const float4*>(lse2 + cb);
-            *reinterpret_cast<float4*>(&lv[4]) = *reinterpret_cast<const float4*>(lse2 + cb + 4);
-            *reinterpret_cast<float4*>(&dd[0]) = *reinterpret_cast<const float4*>(dvec + cb);
-            *reinterpret_cast<float4*>(&dd[4]) = *reinterpret_cast<const float4*>(dvec + cb + 4);
+            // negated lse2 and D of the 8 columns, as 4 packed pairs each
+            const ulonglong2 l01 = *reinterpret_cast<const ulonglong2*>(lse2 + cb);
+            const ulonglong2 l23 = *reinterpret_cast<const ulonglong2*>(lse2 + cb + 4);
+            const ulonglong2 d01 = *reinterpret_cast<const ulonglong2*>(dvec + cb);
+            const ulonglong2 d23 = *reinterpret_cast<const ulonglong2*>(dvec + cb + 4);
+            const uint64_t nl[4] = {l01.x, l01.y, l23.x, l23.y};
+            const uint64_t nd[4] = {d01.x, d01.y, d23.x, d23.y};
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-              float pp[2], ds[2];
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int cl = 2 * e2 + h2;
-                const int c = cb + cl;
-                float pv = ex2_approx(fmaf(__uint_as_float(sr[8 * g8 + cl]), sl2, -lv[cl]));
-                if ((long long)c < lim) pv = 0.f;
-                pp[h2] = pv;
-                ds[h2] = pv * (__uint_as_float(pr[8 * g8 + cl]) - dd[cl]);
+              const int c = cb + 2 * e2;
+              const uint64_t s2 = f2_pack(__uint_as_float(sr[8 * g8 + 2 * e2]),
+                                          __uint_as_float(sr[8 * g8 + 2 * e2 + 1]));
+              const uint64_t dp2 = f2_pack(__uint_as_float(pr[8 * g8 + 2 * e2]),
+                                           __uint_as_float(pr[8 * g8 + 2 * e2 + 1]));
+              float x0, x1;
+              f2_unpack(f2_fma(s2, c2, nl[e2]), x0, x1);
+              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if (masked) {
+                if ((long long)c < lim) p0 = 0.f;
+                if ((long long)c + 1 < lim) p1 = 0.f;
               }
-              pw[4 * g8 + e2] = pack_bf16x2(pp[0], pp[1]);
-              dw[4 * g8 + e2] = pack_bf16x2(ds[0], ds[1]);
+              const uint64_t pp2 = f2_pack(p0, p1);
+              float ds0, ds1;
+              f2_unpack(f2_mul(pp2, f2_add(dp2, nd[e2])), ds0, ds1);
+              pw[4 * g8 + e2] = pack_bf16x2(p0, p1);
+              dw[4 * g8 + e2] = pack_bf16x2(ds0, ds1);
             }
           }
           tmem_st8(tbase + lane_off + C::COL_S + 64 * half + 8 * pass, pw);

@@ -78,8 +78,8 @@ struct BwdArgs {
   int n, T;
   float scale;        // softmax scale
   float scale_log2;   // softmax scale * log2(e)
-  const float* lse;   // lse * log2(e), shard-major [B, H, P, n]
-  const float* Dvec;  // rowsum(dO * O), shard-major [B, H, P, n]
+  const float* lse;   // -lse * log2(e), shard-major [B, H, P, n]
+  const float* Dvec;  // -rowsum(dO * O), shard-major [B, H, P, n]
   float* dq_acc;      // [B, L, H, D] fp32
   void* dk;
   void* dv;

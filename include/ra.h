@@ -134,7 +134,7 @@ ra_status_t ra_bwd(const ra_params_t* p, const void* q, const void* k, const voi
 
 /*
  * The three stages ra_bwd runs, callable one by one (same kernels, same workspace):
- *   ra_bwd_preprocess  D = rowsum(dO * O) and lse * log2(e), both stored shard-major
+ *   ra_bwd_preprocess  D = rowsum(dO * O) and lse * log2(e), both stored negated and shard-major
  *                      ([B, H, P, L/P] fp32) in the workspace; zeroes the fp32 dQ
  *                      accumulator (labhub, "逆伝播での KV 再循環": the D vector).
  *   ra_bwd_main        the ring backward proper: writes dk, dv (bf16) and accumulates
