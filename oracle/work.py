@@ -6,7 +6,11 @@ Assignment of token t (0-based, natural order) to one of P shards of n = L/P tok
 * contiguous -- shard t div n, local index t mod n (vanos001, section "Ring Attention:
   Compute While You Communicate": device i owns the i-th slice of the sequence);
 * striped    -- shard t mod P, local index t div P (vanos001, section "The Causal-Mask
-  Problem: Striped Attention": row r goes to device r mod P).
+  Problem: Striped Attention": row r goes to device r mod P);
+* zigzag     -- the sequence is cut into 2P chunks of c = L/(2P) tokens and shard i holds
+  chunks i and 2P-1-i, in that order (vanos001, same section: each device gets two
+  half-blocks placed symmetrically near the start and the end of the sequence).  Local
+  index a < c is token i*c + a, local index a >= c is token (2P-1-i)*c + (a - c).
 
 Ring order (labhub, section "リング通信パターン"; vanos001 ring diagram): at step k
 shard i works on the KV shard (i - k) mod P, so shard 0 sees 0, P-1, P-2, ..., 1.
@@ -24,22 +28,29 @@ against closed forms and against the printed demo output.
 
 CONTIGUOUS = "contiguous"
 STRIPED = "striped"
+ZIGZAG = "zigzag"
 
 
 def _check_layout(layout):
-    if layout not in (CONTIGUOUS, STRIPED):
-        raise ValueError("layout must be 'contiguous' or 'striped'")
+    if layout not in (CONTIGUOUS, STRIPED, ZIGZAG):
+        raise ValueError("layout must be 'contiguous', 'striped' or 'zigzag'")
 
 
 def shard_of(t, L, P, layout):
     _check_layout(layout)
     n = L // P
+    if layout == ZIGZAG:
+        ch = t // (L // (2 * P))
+        return ch if ch < P else 2 * P - 1 - ch
     return t // n if layout == CONTIGUOUS else t % P
 
 
 def local_of(t, L, P, layout):
     _check_layout(layout)
     n = L // P
+    if layout == ZIGZAG:
+        c = L // (2 * P)
+        return t % c if t // c < P else c + t % c
     return t % n if layout == CONTIGUOUS else t // P
 
 
@@ -49,6 +60,9 @@ def shard_tokens(i, L, P, layout):
     n = L // P
     if layout == CONTIGUOUS:
         return list(range(i * n, (i + 1) * n))
+    if layout == ZIGZAG:
+        c = L // (2 * P)
+        return list(range(i * c, (i + 1) * c)) + list(range((2 * P - 1 - i) * c, (2 * P - i) * c))
     return [a * P + i for a in range(n)]
 
 
@@ -80,6 +94,8 @@ def shard_work(L, P, block, layout, causal):
     _check_layout(layout)
     if L % P or (L // P) % block:
         raise ValueError("seq_len must be divisible by P * block")
+    if layout == ZIGZAG and (L % (2 * P) or (L // (2 * P)) % block):
+        raise ValueError("zigzag needs seq_len divisible by 2 * P * block")
     n = L // P
     T = n // block
     tokens = [shard_tokens(i, L, P, layout) for i in range(P)]

@@ -18,7 +18,7 @@ def _rand(B, L, H, D, seed):
 
 # ---- the method reaches full attention exactly (up to rounding order) -----------
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("P,block", [(1, 8), (2, 4), (4, 2), (4, 8), (8, 4)])
 def test_ring_equals_full_attention(layout, causal, P, block):
@@ -30,7 +30,7 @@ def test_ring_equals_full_attention(layout, causal, P, block):
     assert np.max(np.abs(rl - fl)) < 1e-12
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_merged_partials_equal_full_attention(layout, causal):
     q, k, v = _rand(2, 32, 1, 4, seed=3)
@@ -73,13 +73,14 @@ def test_merge_closed_form_two_equal_partials():
     assert np.max(np.abs(mo - 0.5 * (o[0] + o[1]))) < 1e-15
 
 
+@pytest.mark.parametrize("layout", ["striped", "zigzag"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_striped_permutation_equivariance(causal):
-    """Permute tokens into striped shard-major order, attend with the mask taken on
-    original positions, unpermute: the output equals natural-order attention."""
+def test_permutation_equivariance(layout, causal):
+    """Permute tokens into shard-major order, attend with the mask taken on original
+    positions, unpermute: the output equals natural-order attention."""
     L, P = 48, 4
     q, k, v = _rand(1, L, 1, 8, seed=7)
-    perm = np.concatenate([owork.shard_tokens(i, L, P, "striped") for i in range(P)])
+    perm = np.concatenate([owork.shard_tokens(i, L, P, layout) for i in range(P)])
     qp, kp, vp = q[:, perm], k[:, perm], v[:, perm]
     s = (qp[0, :, 0] @ kp[0, :, 0].T) / np.sqrt(8)
     if causal:
@@ -92,7 +93,7 @@ def test_striped_permutation_equivariance(causal):
     out[perm] = op
     fo, _ = oracle.attention_fwd(q, k, v, causal)
     assert np.max(np.abs(out - fo[0, :, 0])) < 1e-13
-    so, _ = oracle.ring_fwd(q, k, v, P, "striped", causal, block=4)
+    so, _ = oracle.ring_fwd(q, k, v, P, layout, causal, block=2)
     assert np.max(np.abs(so - fo)) < 1e-12
 
 
@@ -109,7 +110,7 @@ def test_ring_order_golden():
                 assert order[kk] == int(want), (dev, kk)
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 def test_assignment_is_a_partition(layout):
     L, P = 96, 8
     seen = sorted(t for i in range(P) for t in oracle.shard_tokens(i, L, P, layout))
@@ -117,6 +118,13 @@ def test_assignment_is_a_partition(layout):
     for t in range(L):
         i, a = oracle.shard_of(t, L, P, layout), oracle.local_of(t, L, P, layout)
         assert oracle.shard_tokens(i, L, P, layout)[a] == t
+
+
+def test_zigzag_holds_symmetric_chunks():
+    # L = 16, P = 4: chunks of 2; shard 1 holds chunk 1 (tokens 2, 3) and chunk 6 (12, 13)
+    assert oracle.shard_tokens(1, 16, 4, "zigzag") == [2, 3, 12, 13]
+    assert [oracle.shard_of(t, 16, 4, "zigzag") for t in range(16)] == \
+        [0, 0, 1, 1, 2, 2, 3, 3, 3, 3, 2, 2, 1, 1, 0, 0]
 
 
 def test_striped_is_round_robin():
@@ -157,6 +165,18 @@ def test_work_model_closed_forms(L, P, block):
     assert sum(c["pairs"]) == sum(s["pairs"]) == L * (L + 1) // 2
     nc = oracle.shard_work(L, P, block, "striped", causal=False)
     assert nc["tiles"] == [P * T * T] * P and nc["pairs"] == [n * L] * P
+
+
+@pytest.mark.parametrize("L,P,block", [(64, 4, 4), (256, 8, 8), (512, 4, 16), (256, 2, 64)])
+def test_zigzag_work_is_balanced_in_closed_form(L, P, block):
+    c = L // (2 * P)
+    Tc = c // block
+    z = oracle.shard_work(L, P, block, "zigzag", causal=True)
+    for i in range(P):
+        assert z["pairs"][i] == c * c * (2 * P - 1) + c * (c + 1)
+        assert z["tiles"][i] == Tc * Tc * (2 * P - 1) + Tc * (Tc + 1)
+    assert sum(z["pairs"]) == L * (L + 1) // 2
+    assert len(set(z["visits"])) == 1
 
 
 def test_striped_balance_at_the_workload_shapes():
