@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libra.so")
 HEADER_PATH = os.path.join(_HERE, "..", "include", "ra.h")
 
-LAYOUTS = {"contiguous": 0, "striped": 1}
+LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
 STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_WORKSPACE",
           4: "RA_ERR_CUDA", 5: "RA_ERR_DEVICE_TIMEOUT"}
 RA_BF16, RA_FP32 = 0, 1

@@ -34,11 +34,17 @@ ra_status_t check_params(const ra_params_t* p, bool gpu_shapes) {
     return fail(RA_ERR_INVALID_ARG, "batch, heads, seq_len and P must be >= 1");
   if (p->P > 1024) return fail(RA_ERR_INVALID_ARG, "P must be <= 1024");
   if (p->block < 1) return fail(RA_ERR_INVALID_ARG, "block must be >= 1");
-  if (p->layout != RA_LAYOUT_CONTIGUOUS && p->layout != RA_LAYOUT_STRIPED)
-    return fail(RA_ERR_INVALID_ARG, "layout must be RA_LAYOUT_CONTIGUOUS or RA_LAYOUT_STRIPED");
+  if (p->layout != RA_LAYOUT_CONTIGUOUS && p->layout != RA_LAYOUT_STRIPED &&
+      p->layout != RA_LAYOUT_ZIGZAG)
+    return fail(RA_ERR_INVALID_ARG,
+                "layout must be RA_LAYOUT_CONTIGUOUS, RA_LAYOUT_STRIPED or RA_LAYOUT_ZIGZAG");
   if (p->causal != 0 && p->causal != 1) return fail(RA_ERR_INVALID_ARG, "causal must be 0 or 1");
   if (p->seq_len % p->P != 0 || (p->seq_len / p->P) % p->block != 0)
     return fail(RA_ERR_INVALID_ARG, "seq_len (%lld) must be divisible by P * block (%d * %d)",
+                (long long)p->seq_len, p->P, p->block);
+  if (p->layout == RA_LAYOUT_ZIGZAG && (p->seq_len / p->P) % (2LL * p->block) != 0)
+    return fail(RA_ERR_INVALID_ARG,
+                "zigzag: seq_len (%lld) must be divisible by 2 * P * block (2 * %d * %d)",
                 (long long)p->seq_len, p->P, p->block);
   if (!gpu_shapes) return RA_OK;
   if (p->head_dim < 1) return fail(RA_ERR_INVALID_ARG, "head_dim must be >= 1");
@@ -118,9 +124,11 @@ EncodeTiledFn encode_fn() {
 
 // A bf16 [B, L, H, D] tensor viewed as 5-D so that one box is `box_rows` consecutive
 // local rows of one shard and 64 features of one head (128-byte swizzled rows):
-//   striped    dims (D, H, P, n, B): token = local * P + shard
-//   contiguous dims (D, H, n, P, B): token = shard * n + local
-// (strides increase with the dimension index in both views).
+//   striped    dims (D, H, P, n, B):  token = local * P + shard
+//   contiguous dims (D, H, n, P, B):  token = shard * n + local
+//   zigzag     dims (D, H, c, 2P, B): token = chunk * c + row, c = n / 2 (the kernels
+//              pick chunk = shard or 2P-1-shard from the local row)
+// (strides increase with the dimension index in every view).
 ra_status_t make_rows_map(CUtensorMap* m, const void* base, const ra_params_t* p, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
@@ -144,10 +152,11 @@ ra_status_t make_rows_map(CUtensorMap* m, const void* base, const ra_params_t* p
     box[2] = 1;
     box[3] = box_rows;
   } else {
-    dims[2] = n;
-    dims[3] = P;
+    const cuuint64_t rows = (p->layout == RA_LAYOUT_ZIGZAG) ? n / 2 : n;
+    dims[2] = rows;
+    dims[3] = L / rows;
     strides[1] = H * D * 2;
-    strides[2] = n * H * D * 2;
+    strides[2] = rows * H * D * 2;
     box[2] = box_rows;
     box[3] = 1;
   }
@@ -179,15 +188,17 @@ void work_model(const ra_params_t* p, unsigned long long* outp) {
         t += (unsigned long long)(Tb * (Tb + 1) / 2);
         pr += (j <= i) ? sum_a + R : sum_a;
       } else {
-        for (long long tb = 0; tb < Tb; ++tb) {
-          long long c = (long long)(i - j) * Tb + tb + 1;
-          t += c < 0 ? 0 : (c > Tb ? Tb : c);
-        }
-        pr += (j < i) ? R * n : (j == i ? sum_a + R : 0ull);
+        for (long long tb = 0; tb < Tb; ++tb)
+          t += blocks_upto(p->layout, j, block_pos(p->layout, i, tb, Tb, P), Tb, P);
+        if (p->layout == RA_LAYOUT_CONTIGUOUS)
+          pr += (j < i) ? R * n : (j == i ? sum_a + R : 0ull);
+        else
+          for (long long r = 0; r < n; ++r)
+            pr += tokens_upto(p->layout, j, token_of(p->layout, i, r, n, P), n, P);
       }
     }
     for (long long r = 0; r < n; ++r) {
-      const long long tok = (p->layout == RA_LAYOUT_STRIPED) ? r * P + i : (long long)i * n + r;
+      const long long tok = token_of(p->layout, i, r, n, P);
       v += p->causal ? (unsigned long long)(tok / blk + 1) : (unsigned long long)(L / blk);
     }
     tiles[i] = t;

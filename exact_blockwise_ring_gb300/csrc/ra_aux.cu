@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(256)
     const long long tok = bl % L;
     const int b = (int)(bl / L);
     const long long n = L / P;
-    const long long shard = (layout == RA_LAYOUT_STRIPED) ? tok % P : tok / n;
-    const long long local = (layout == RA_LAYOUT_STRIPED) ? tok / P : tok % n;
+    long long shard, local;
+    shard_local_of(layout, tok, n, P, &shard, &local);
     const size_t bh = (size_t)b * H + h;
     const size_t dst = (bh * P + shard) * n + local;
     Dsm[dst] = -acc;

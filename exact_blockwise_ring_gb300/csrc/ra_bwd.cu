@@ -36,6 +36,7 @@
 
 #include "ra_internal.h"
 #include "ra_ptx.cuh"
+#include "ra_rows.cuh"
 
 namespace ra {
 
@@ -69,15 +70,6 @@ struct BwdCfg {
 
 constexpr uint32_t kErrMisaligned = 0x10u;
 
-__device__ __forceinline__ void load_rows(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                          int layout, int d0, int h, int shard, int local0,
-                                          int b) {
-  if (layout == RA_LAYOUT_STRIPED)
-    tma_load_5d(dst, m, bar, d0, h, shard, local0, b);
-  else
-    tma_load_5d(dst, m, bar, d0, h, local0, shard, b);
-}
-
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
@@ -106,23 +98,25 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
 
 // Query tiles of shard i that see KV tile (j, u): for query tile t (128 rows),
 //   key row b (0..127) is visible to query row a (0..127) iff a - b + delta >= 0 with
-//   contiguous: delta = (i - j) * n + 128 (t - u)
-//   striped:    delta = 128 (t - u) - (i < j)
-// skip: delta < -127; full: delta >= 127 (or non-causal); otherwise masked.
+//   contiguous, zigzag: delta = 128 (block_pos(i, t) - block_pos(j, u))
+//   striped:            delta = 128 (t - u) - (i < j)
+// skip: delta < -127; full: delta >= 127 (or non-causal); otherwise masked.  Tile
+// positions grow with t, so the visible query tiles of a shard are a suffix t >= t_lo.
 struct BwdSched {
   int j, u, n, T, P, layout, causal;
   __device__ int i_of(int k) const { return (j + k) % P; }
   __device__ long long delta(int i, int t) const {
     if (layout == RA_LAYOUT_STRIPED) return 128LL * (t - u) - (i < j ? 1 : 0);
-    return (long long)(i - j) * n + 128LL * (t - u);
+    return 128LL * (block_pos(layout, i, t, T, P) - block_pos(layout, j, u, T, P));
   }
   // first query tile with delta >= -127
   __device__ int t_lo(int i) const {
     if (!causal) return 0;
-    long long num = (layout == RA_LAYOUT_STRIPED) ? 128LL * u + (i < j ? 1 : 0) - 127
-                                                  : 128LL * u - (long long)(i - j) * n - 127;
+    if (layout != RA_LAYOUT_STRIPED)
+      return (int)blocks_upto(layout, i, block_pos(layout, j, u, T, P) - 1, T, P);
+    const long long num = 128LL * u + (i < j ? 1 : 0) - 127;
     if (num <= 0) return 0;
-    long long t = (num + 127) / 128;
+    const long long t = (num + 127) / 128;
     return t > T ? T : (int)t;
   }
 };
@@ -174,6 +168,11 @@ __global__ void __launch_bounds__(640, 1)
   if (a.layout == RA_LAYOUT_STRIPED || !a.causal) {
     u = idx / a.P;
     j = idx % a.P;
+  } else if (a.layout == RA_LAYOUT_ZIGZAG) {
+    // idx = natural-order position of the KV tile (smallest first = most query tiles)
+    const int th = a.T >> 1, ch = idx / th;
+    j = ch < a.P ? ch : 2 * a.P - 1 - ch;
+    u = idx % th + (ch < a.P ? 0 : th);
   } else {
     j = idx / a.T;
     u = idx % a.T;
@@ -217,8 +216,10 @@ __global__ void __launch_bounds__(640, 1)
       tma_prefetch_desc(&tmDO);
       mbar_expect_tx(kv_full, 2 * C::KB);
       for (int cb = 0; cb < 2; ++cb) {
-        load_rows(sK + cb * kTile * 128, &tmK, kv_full, a.layout, cb * 64, h, j, u * kTile, b);
-        load_rows(sV + cb * kTile * 128, &tmV, kv_full, a.layout, cb * 64, h, j, u * kTile, b);
+        load_rows(sK + cb * kTile * 128, &tmK, kv_full, a.layout, cb * 64, h, j, u * kTile, b,
+                  a.n, a.P);
+        load_rows(sV + cb * kTile * 128, &tmV, kv_full, a.layout, cb * 64, h, j, u * kTile, b,
+                  a.n, a.P);
       }
       int m = 0;
       bool ok = true;
@@ -230,9 +231,9 @@ __global__ void __launch_bounds__(640, 1)
           mbar_expect_tx(&q_full[st], 2 * C::QB + C::LDB);
           for (int cb = 0; cb < 2; ++cb) {
             load_rows(sQ + st * C::QB + cb * BQ * 128, &tmQ, &q_full[st], a.layout, cb * 64, h, i,
-                      t * BQ, b);
+                      t * BQ, b, a.n, a.P);
             load_rows(sDO + st * C::QB + cb * BQ * 128, &tmDO, &q_full[st], a.layout, cb * 64, h,
-                      i, t * BQ, b);
+                      i, t * BQ, b, a.n, a.P);
           }
           const size_t off = ld_base + (size_t)i * a.n + (size_t)t * BQ;
           bulk_load(sLD + st * (2 * BQ), a.lse + off, BQ * 4, &q_full[st]);
@@ -423,8 +424,7 @@ __global__ void __launch_bounds__(640, 1)
     if (ok && mbar_wait(kv_final, 0, wc)) {
       tc_fence_after();
       const int loc = u * kTile + brow;
-      const long long tok = (a.layout == RA_LAYOUT_STRIPED) ? (long long)loc * a.P + j
-                                                          : (long long)j * a.n + loc;
+      const long long tok = token_of(a.layout, j, loc, a.n, a.P);
       const size_t row = ((size_t)b * a.L + tok) * a.H + h;
       const bool any = m > 0;
       const uint32_t tcol = tbase + lane_off + (half ? C::COL_DK : C::COL_DV);
@@ -469,9 +469,8 @@ __global__ void __launch_bounds__(640, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(dq_empty);
-        const long long tok0 = (a.layout == RA_LAYOUT_STRIPED)
-                                   ? (long long)(t * BQ + 64 * half) * a.P + i
-                                   : (long long)i * a.n + t * BQ + 64 * half;
+        // 64 consecutive local rows: consecutive tokens (stride qstride) in every layout
+        const long long tok0 = token_of(a.layout, i, t * BQ + 64 * half, a.n, a.P);
         float* p0 = dq_head + tok0 * a.H * D_;
 #pragma unroll
         for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * qstride, __uint_as_float(q0[c]));

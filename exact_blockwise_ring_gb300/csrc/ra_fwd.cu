@@ -35,6 +35,7 @@
 
 #include "ra_internal.h"
 #include "ra_ptx.cuh"
+#include "ra_rows.cuh"
 
 namespace ra {
 
@@ -64,15 +65,6 @@ struct FwdCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ void load_rows(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                          int layout, int d0, int h, int shard, int local0,
-                                          int b) {
-  if (layout == RA_LAYOUT_STRIPED)
-    tma_load_5d(dst, m, bar, d0, h, shard, local0, b);
-  else
-    tma_load_5d(dst, m, bar, d0, h, local0, shard, b);
-}
-
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
                                                 uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
@@ -99,24 +91,24 @@ __device__ void count_work(const FwdArgs& a, const RingSched& sc, int g) {
     for (int tb = r0 / a.block; tb * a.block < r1; ++tb) {
       if (!a.causal) n_tiles += Tb;
       else if (a.layout == RA_LAYOUT_STRIPED) n_tiles += tb + 1;
-      else {
-        long long c = (long long)(i - j) * Tb + tb + 1;
-        n_tiles += c < 0 ? 0 : (c > Tb ? Tb : c);
-      }
+      else n_tiles += blocks_upto(a.layout, j, block_pos(a.layout, i, tb, Tb, a.P), Tb, a.P);
     }
     const unsigned long long R = r1 - r0;
     const unsigned long long sum_a = R * r0 + R * (R - 1) / 2;   // sum of local rows a
     if (!a.causal) n_pairs += R * a.n;
     else if (a.layout == RA_LAYOUT_STRIPED) n_pairs += (j <= i) ? sum_a + R : sum_a;
-    else n_pairs += (j < i) ? R * a.n : (j == i ? sum_a + R : 0ull);
+    else if (a.layout == RA_LAYOUT_CONTIGUOUS)
+      n_pairs += (j < i) ? R * a.n : (j == i ? sum_a + R : 0ull);
+    else   // zigzag: row by row
+      for (int r = r0; r < r1; ++r)
+        n_pairs += tokens_upto(a.layout, j, token_of(a.layout, i, r, a.n, a.P), a.n, a.P);
   }
   atomicAdd(&tiles[i], n_tiles);
   atomicAdd(&pairs[i], n_pairs);
   if (g == 0) {
     unsigned long long v = 0;
     for (int r = r0; r < r1; ++r) {
-      const long long tok = (a.layout == RA_LAYOUT_STRIPED) ? (long long)r * a.P + i
-                                                            : (long long)i * a.n + r;
+      const long long tok = token_of(a.layout, i, r, a.n, a.P);
       v += a.causal ? (unsigned long long)(tok / a.block + 1)
                     : (unsigned long long)(a.L / a.block);
     }
@@ -154,7 +146,8 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- decode this CTA: one (batch, head) after another so that the CTAs resident at
-  // any time share that head's K/V in L2; inside a head, heavy work first --------------
+  // any time share that head's K/V in L2; inside a head, heavy work first (for the
+  // blocked layouts: tile pairs in descending natural-order position) ------------------
   const int per_bh = a.n_split * a.P * a.npair;
   const int bh = blockIdx.x / per_bh;
   int idx = blockIdx.x % per_bh;
@@ -165,6 +158,13 @@ __global__ void __launch_bounds__(384, 1)
     const int pos = a.P * a.npair - 1 - idx;
     i = pos / a.npair;
     s = pos % a.npair;
+  } else if (a.causal && a.layout == RA_LAYOUT_ZIGZAG && (a.T & 3) == 0) {
+    // T/2 tiles per chunk, an even number: T/4 pairs per chunk, none straddles two
+    const int hp = a.T >> 2;
+    const int pos = a.P * a.npair - 1 - idx;
+    const int ch = pos / hp;
+    i = ch < a.P ? ch : 2 * a.P - 1 - ch;
+    s = (ch < a.P ? 0 : hp) + pos % hp;
   } else {
     s = a.npair - 1 - idx / a.P;
     i = idx % a.P;
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int q = 0; q < nvalid; ++q)
           for (int cb = 0; cb < C::NCB; ++cb)
             load_rows(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h, i,
-                      (2 * s + q) * kTile, b);
+                      (2 * s + q) * kTile, b, a.n, a.P);
       }
       int n = 0;
       bool ok = true;
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_expect_tx(&full[st], C::KVB);
           for (int cb = 0; cb < C::NCB; ++cb)
             load_rows(ring + st * C::KVB + cb * kTile * 128, tm, &full[st], a.layout, cb * 64, h,
-                      j, u * kTile, b);
+                      j, u * kTile, b, a.n, a.P);
         }
       }
       // let every copy this thread issued land before the CTA can exit
@@ -433,8 +433,7 @@ __global__ void __launch_bounds__(384, 1)
     if (ok && mbar_wait(&o_final[q], 0, wc) && valid) {
       tc_fence_after();
       const int loc = t * kTile + arow;
-      const long long tok = (a.layout == RA_LAYOUT_STRIPED) ? (long long)loc * a.P + i
-                                                          : (long long)i * a.n + loc;
+      const long long tok = token_of(a.layout, i, loc, a.n, a.P);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_v =
           l_run > 0.f ? (m_run * sl2 + __log2f(l_run)) * 0.69314718055994531f : kNegInf;

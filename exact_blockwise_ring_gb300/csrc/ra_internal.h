@@ -21,13 +21,81 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 enum TileClass : int { kSkip = 0, kFull = 1, kDiag = 2 };
 
+// ---- token assignment (n = L / P tokens per shard) ----------------------------------
+//   contiguous: local row a of shard i is token i*n + a
+//   striped:    token a*P + i
+//   zigzag:     2P chunks of c = n/2 tokens; rows [0, c) are chunk i, rows [c, 2c) are
+//               chunk 2P-1-i (vanos001, section "The Causal-Mask Problem: Striped
+//               Attention": two half-shards placed symmetrically near the two ends)
+__host__ __device__ inline long long token_of(int layout, int i, long long a, long long n,
+                                              int P) {
+  if (layout == RA_LAYOUT_STRIPED) return a * P + i;
+  if (layout == RA_LAYOUT_ZIGZAG) {
+    const long long c = n >> 1;
+    return a < c ? (long long)i * c + a : (2LL * P - 1 - i) * c + (a - c);
+  }
+  return (long long)i * n + a;
+}
+
+__host__ __device__ inline void shard_local_of(int layout, long long tok, long long n, int P,
+                                               long long* shard, long long* local) {
+  if (layout == RA_LAYOUT_STRIPED) {
+    *shard = tok % P;
+    *local = tok / P;
+  } else if (layout == RA_LAYOUT_ZIGZAG) {
+    const long long c = n >> 1, ch = tok / c;
+    *shard = ch < P ? ch : 2LL * P - 1 - ch;
+    *local = tok % c + (ch < P ? 0 : c);
+  } else {
+    *shard = tok / n;
+    *local = tok % n;
+  }
+}
+
+// For the blocked layouts (contiguous, zigzag): natural-order position of block t of
+// shard i, counted in blocks of the same size (T blocks per shard, T even for zigzag).
+// It increases with t, so the blocks of a shard that lie at or before a position g form
+// a prefix, of length blocks_upto().
+__host__ __device__ inline long long block_pos(int layout, int i, long long t, long long T,
+                                               int P) {
+  if (layout == RA_LAYOUT_ZIGZAG) {
+    const long long Th = T >> 1;
+    return t < Th ? (long long)i * Th + t : (2LL * P - 1 - i) * Th + (t - Th);
+  }
+  return (long long)i * T + t;
+}
+
+__host__ __device__ inline long long clamp_ll(long long x, long long lo, long long hi) {
+  return x < lo ? lo : (x > hi ? hi : x);
+}
+
+// Number of blocks t of shard i with block_pos(i, t) <= g.
+__host__ __device__ inline long long blocks_upto(int layout, int i, long long g, long long T,
+                                                 int P) {
+  if (layout == RA_LAYOUT_ZIGZAG) {
+    const long long Th = T >> 1;
+    return clamp_ll(g - (long long)i * Th + 1, 0, Th) +
+           clamp_ll(g - (2LL * P - 1 - i) * Th + 1, 0, Th);
+  }
+  return clamp_ll(g - (long long)i * T + 1, 0, T);
+}
+
+// Number of tokens of shard j at or before token `tok` (any layout).
+__host__ __device__ inline long long tokens_upto(int layout, int j, long long tok, long long n,
+                                                 int P) {
+  if (layout == RA_LAYOUT_STRIPED) return tok < j ? 0 : clamp_ll((tok - j) / P + 1, 0, n);
+  return blocks_upto(layout, j, tok, n, P);   // blocks of one token
+}
+
 // Ring schedule of one query-side unit of work: the query rows are the local 128-row
 // tiles t0 .. t0+nq-1 of shard i; ring steps k0 .. k1-1 visit KV shard j = (i - k) mod P,
 // and inside a step the KV tiles u = 0 .. u_end(j)-1 of that shard in order.
 // Causal classification (per 128 x 128 tile, original token positions):
-//   contiguous: global tiles gq = i*T + t, gk = j*T + u; skip gk > gq, diag gk == gq;
+//   contiguous, zigzag: natural-order tile positions gq = block_pos(i, t),
+//               gk = block_pos(j, u); skip gk > gq, diag gk == gq (mask b <= a);
 //   striped:    skip u > t, diag u == t (mask inside: key b visible to query a iff
 //               b < a, or b == a and j <= i), full u < t.
+// In every layout the visible KV tiles of a shard form a prefix u < u_end(j).
 struct RingSched {
   int i, t0, nq, T, P, layout, causal, k0, k1;
 
@@ -40,16 +108,14 @@ struct RingSched {
     int tmax = t0 + nq - 1;
     if (tmax > T - 1) tmax = T - 1;
     if (layout == RA_LAYOUT_STRIPED) return tmax + 1;
-    long long lim = (long long)(i - j) * T + tmax;
-    if (lim < 0) return 0;
-    return lim >= T ? T : (int)lim + 1;
+    return (int)blocks_upto(layout, j, block_pos(layout, i, tmax, T, P), T, P);
   }
   __host__ __device__ int cls(int q, int j, int u) const {
     const int t = t0 + q;
     if (q >= nq || t >= T) return kSkip;
     if (!causal) return kFull;
     if (layout == RA_LAYOUT_STRIPED) return u < t ? kFull : (u == t ? kDiag : kSkip);
-    const long long gq = (long long)i * T + t, gk = (long long)j * T + u;
+    const long long gq = block_pos(layout, i, t, T, P), gk = block_pos(layout, j, u, T, P);
     return gk < gq ? kFull : (gk == gq ? kDiag : kSkip);
   }
 };

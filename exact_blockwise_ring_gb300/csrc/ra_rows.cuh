@@ -1,0 +1,30 @@
+// ra_rows.cuh -- TMA load of 128 consecutive local rows of one shard, for every layout.
+#pragma once
+
+#include "ra_internal.h"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+// The host views each bf16 [B, L, H, D] tensor as 5-D so that one box is 128 rows of one
+// shard and 64 features of one head (make_rows_map):
+//   striped    dims (D, H, P, n, B):   coordinates (d0, h, shard, local, b)
+//   contiguous dims (D, H, n, P, B):   coordinates (d0, h, local, shard, b)
+//   zigzag     dims (D, H, c, 2P, B):  coordinates (d0, h, local mod c, chunk, b), with
+//              chunk = shard for local < c and 2P-1-shard otherwise; c = n/2 is a multiple
+//              of 128, so a box never straddles the two chunks.
+__device__ __forceinline__ void load_rows(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                          int layout, int d0, int h, int shard, int local0,
+                                          int b, int n, int P) {
+  if (layout == RA_LAYOUT_STRIPED) {
+    tma_load_5d(dst, m, bar, d0, h, shard, local0, b);
+  } else if (layout == RA_LAYOUT_ZIGZAG) {
+    const int c = n >> 1;
+    const bool lo = local0 < c;
+    tma_load_5d(dst, m, bar, d0, h, lo ? local0 : local0 - c, lo ? shard : 2 * P - 1 - shard, b);
+  } else {
+    tma_load_5d(dst, m, bar, d0, h, local0, shard, b);
+  }
+}
+
+}  // namespace ra

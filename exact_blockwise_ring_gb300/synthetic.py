@@ -13,13 +13,13 @@ WORKLOADS = {
     "tiny":  dict(batch=1, heads=2, head_dim=64, seq_len=512, P=4, block=128,
                   causal=False, layouts=("contiguous",), backward=False),
     "8k":    dict(batch=1, heads=8, head_dim=128, seq_len=8192, P=8, block=128,
-                  causal=True, layouts=("contiguous", "striped"), backward=False),
+                  causal=True, layouts=("contiguous", "striped", "zigzag"), backward=False),
     "32k":   dict(batch=1, heads=32, head_dim=128, seq_len=32768, P=8, block=128,
-                  causal=True, layouts=("striped",), backward=True),
+                  causal=True, layouts=("striped", "zigzag"), backward=True),
     "262k":  dict(batch=1, heads=32, head_dim=128, seq_len=262144, P=16, block=256,
-                  causal=True, layouts=("striped",), backward=True),
+                  causal=True, layouts=("striped", "zigzag"), backward=True),
     "1m":    dict(batch=1, heads=8, head_dim=128, seq_len=1048576, P=32, block=256,
-                  causal=True, layouts=("striped", "contiguous"), backward=True),
+                  causal=True, layouts=("striped", "contiguous", "zigzag"), backward=True),
 }
 
 SEEDS = {"tiny": 1000, "8k": 1001, "32k": 1002, "262k": 1003, "1m": 1004}

@@ -1,6 +1,6 @@
 /*
- * ra.h -- C ABI of libra: exact blockwise ring attention (contiguous and striped
- * layouts) over P virtual shards held on one GPU, for NVIDIA GB300 (sm_103a).
+ * ra.h -- C ABI of libra: exact blockwise ring attention (contiguous, striped and
+ * zigzag layouts) over P virtual shards held on one GPU, for NVIDIA GB300 (sm_103a).
  *
  * The method (sources are four web pages on Ring Attention / Striped Attention):
  *   - "Ring Attention 論文分析" (labhub): blockwise attention with an online softmax
@@ -11,14 +11,16 @@
  *   - "Ring Attention: Sequence Parallelism for Long Context" (vanos001): ring order
  *     (step k: shard i attends KV shard (i - k) mod P), the striped assignment
  *     (token r -> shard r mod P, section "The Causal-Mask Problem: Striped
- *     Attention"), and the per-device work count of section "Worked Demo".
+ *     Attention"), the zigzag assignment (same section: two half-shards placed
+ *     symmetrically near the start and the end of the sequence), and the per-device
+ *     work count of section "Worked Demo".
  *
  * One call covers all P shards: the pages' per-device ring becomes a schedule inside
  * one kernel, and a "hop" is a tile load of KV shard (i - k) mod P from device memory.
  *
  * Conventions for every entry point:
  *   - Tensors are row-major.  q, k, v, out, dout, dq, dk, dv are [B, L, H, D] with
- *     tokens in NATURAL order for both layouts (the shard permutation is internal;
+ *     tokens in NATURAL order for every layout (the shard permutation is internal;
  *     attention is permutation-equivariant, aibr.jp Striped Attention summary, §3).
  *     lse is float32 [B, H, L], natural logarithm.
  *   - All pointers are DEVICE pointers unless stated otherwise, 16-byte aligned.
@@ -51,7 +53,11 @@ typedef enum {
   RA_ERR_DEVICE_TIMEOUT = 5   /* a bounded wait inside a kernel ran out           */
 } ra_status_t;
 
-typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1 } ra_layout_t;
+typedef enum {
+  RA_LAYOUT_CONTIGUOUS = 0,
+  RA_LAYOUT_STRIPED = 1,
+  RA_LAYOUT_ZIGZAG = 2
+} ra_layout_t;
 typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype_t;
 
 /*
@@ -59,14 +65,16 @@ typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype_t;
  *   batch, heads     B, H >= 1.
  *   seq_len          L >= 1, divisible by P * block (the pages assume equal shards,
  *                    labhub section "長文データの前処理とチャンク割り当て"; there is
- *                    no padding here).
+ *                    no padding here); ZIGZAG needs L divisible by 2 * P * block.
  *   head_dim         D in {64, 128}.
  *   block            the blockwise loop's block size (BPT block_size), {128, 256}.
  *                    The result does not depend on it beyond rounding order; it sets
  *                    the unit of the work counter's "tiles".
  *   P                number of virtual shards (ring length), 1 <= P <= 1024.
- *   layout           ra_layout_t: CONTIGUOUS (token t -> shard t / (L/P)) or
- *                    STRIPED (token t -> shard t mod P).
+ *   layout           ra_layout_t: CONTIGUOUS (token t -> shard t / (L/P)),
+ *                    STRIPED (token t -> shard t mod P) or ZIGZAG (the sequence cut
+ *                    into 2P chunks of c = L/(2P) tokens; shard i holds chunks i and
+ *                    2P-1-i, local rows [0, c) and [c, 2c) in that order).
  *   causal           0 or 1 (key c visible to query r iff c <= r, original positions).
  *   softmax_scale    > 0, or 0 for 1/sqrt(D).
  *   n_split          forward only: 1 = one online-softmax state carried over all P

@@ -58,7 +58,8 @@ def _fwd(L, prm, q=FAKE, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30, odt=0, s
     (dict(P=2000, seq_len=2000 * 128), 1),
     (dict(head_dim=96), 2),               # valid, no kernel
     (dict(block=64, seq_len=1024), 2),
-    (dict(layout=2), 1),
+    (dict(layout=3), 1),
+    (dict(layout=2, seq_len=4 * 128 * 3), 1),   # zigzag: L / P not a multiple of 2 * block
     (dict(causal=3), 1),
     (dict(softmax_scale=-1.0), 1),
     (dict(softmax_scale=float("inf")), 1),
@@ -125,9 +126,10 @@ def test_work_model_reproduces_demo(L):
         assert w["visits"] == rows[layout]
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("L_,P,block", [(64, 4, 4), (512, 8, 16), (1024, 2, 128), (2048, 4, 256)])
+@pytest.mark.parametrize("L_,P,block", [(64, 4, 4), (512, 8, 16), (1024, 2, 128), (2048, 4, 256),
+                                        (96, 3, 4)])
 def test_work_model_matches_oracle(L, layout, causal, L_, P, block):
     got = era.ra_shard_work_model(L_, P, block, layout, causal)
     want = oracle.shard_work(L_, P, block, layout, causal)

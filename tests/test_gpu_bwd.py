@@ -43,6 +43,11 @@ SWEEP = [
     (1, 1024, 1, 1, 128, "contiguous", True),     # P = 1
     (1, 1024, 2, 4, 128, "contiguous", False),
     (1, 1024, 2, 4, 128, "striped", False),
+    (1, 1024, 2, 4, 128, "zigzag", True),         # one tile per chunk
+    (2, 2048, 3, 2, 128, "zigzag", True),
+    (1, 1536, 2, 2, 128, "zigzag", True),         # 3 tiles per chunk
+    (1, 2048, 2, 4, 256, "zigzag", True),
+    (1, 1024, 2, 4, 128, "zigzag", False),
 ]
 
 
@@ -75,8 +80,10 @@ def test_bwd_layouts_agree():
     q, k, v, do = make_inputs(1, 4096, 2, 128, seed=22)
     a = _run(q, k, v, do, 8, 128, "contiguous", True)
     b = _run(q, k, v, do, 8, 128, "striped", True)
-    for x, y in zip(a, b):
+    z = _run(q, k, v, do, 8, 128, "zigzag", True)
+    for x, y, w in zip(a, b, z):
         assert float((x.float() - y.float()).norm() / y.float().norm()) <= GRAD_TOL
+        assert float((w.float() - y.float()).norm() / y.float().norm()) <= GRAD_TOL
 
 
 def test_bwd_unsupported_head_dim():

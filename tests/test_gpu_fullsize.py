@@ -28,7 +28,8 @@ def _rows(L, P, layout):
     return sorted(r for r in picks if 0 <= r < L)
 
 
-CASES = [("32k", "striped"), ("262k", "striped"), ("1m", "striped"), ("1m", "contiguous")]
+CASES = [("32k", "striped"), ("262k", "striped"), ("1m", "striped"), ("1m", "contiguous"),
+         ("32k", "zigzag"), ("1m", "zigzag")]
 
 
 @pytest.mark.parametrize("name,layout", CASES)

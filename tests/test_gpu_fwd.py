@@ -59,6 +59,12 @@ SWEEP = [
     (1, 2048, 2, 128, 4, 128, "striped", True, 2),      # split into partials + merge
     (1, 2048, 2, 128, 4, 128, "contiguous", True, 4),
     (1, 2048, 2, 64, 4, 128, "striped", True, 4),
+    (1, 1024, 2, 128, 2, 128, "zigzag", True, 1),       # 2 tiles per chunk
+    (2, 2048, 3, 128, 4, 128, "zigzag", True, 1),
+    (1, 1536, 2, 128, 2, 128, "zigzag", True, 1),       # 3 tiles per chunk: a pair straddles
+    (1, 2048, 2, 64, 4, 256, "zigzag", True, 1),
+    (1, 2048, 2, 128, 4, 128, "zigzag", True, 2),
+    (1, 1024, 2, 128, 4, 128, "zigzag", False, 1),
 ]
 
 
@@ -83,7 +89,7 @@ def test_fwd_tiny_workload():
             assert eo <= OUT_TOL and el <= LSE_TOL, (layout, n_split, eo, el)
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 def test_fwd_8k_workload(layout):
     w = WORKLOADS["8k"]
     qkv, (q64, k64, v64) = _case(w["batch"], w["seq_len"], w["heads"], w["head_dim"], SEEDS["8k"])
@@ -95,7 +101,7 @@ def test_fwd_8k_workload(layout):
     ob, _ = _gpu_fwd(qkv, w["P"], w["block"], layout, True, out_dtype=torch.bfloat16)
     diff = np.abs(ob.float().cpu().numpy() - o_ref)
     assert np.all(diff <= OUT_TOL + 2.0 ** -8 * np.abs(o_ref))
-    # per-shard work: device counters == host closed form; striped is balanced
+    # per-shard work: device counters == host closed form; striped, zigzag are balanced
     model = era.ra_shard_work_model(w["seq_len"], w["P"], w["block"], layout, True)
     got = sw.cpu().numpy().astype(np.int64)
     H = w["heads"]
@@ -103,13 +109,13 @@ def test_fwd_8k_workload(layout):
         assert list(got[u]) == [H * x for x in model[name]], name
     pairs = got[1].astype(np.float64)
     ratio = pairs.max() / pairs.mean()
-    if layout == "striped":
+    if layout != "contiguous":
         assert ratio <= 1.05
     else:
         assert ratio > 1.5
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 def test_first_causal_token_is_exact(layout):
     qkv, (q64, k64, v64) = _case(2, 1024, 2, 128, seed=5)
     out, lse = _gpu_fwd(qkv, 4, 128, layout, True)
@@ -122,7 +128,7 @@ def test_first_causal_token_is_exact(layout):
 def test_constant_v_gives_constant_output():
     q, k, _ = make_inputs(1, 2048, 2, 128, seed=6, with_dout=False)
     v = torch.linspace(-2, 3, 128).to(torch.bfloat16).expand(1, 2048, 2, 128).contiguous()
-    for layout in ("contiguous", "striped"):
+    for layout in ("contiguous", "striped", "zigzag"):
         out, _ = _gpu_fwd((q, k, v), 8, 128, layout, True)
         assert float((out.cpu() - v.float()).abs().max()) <= OUT_TOL
 
@@ -135,6 +141,9 @@ def test_layouts_agree_and_runs_are_deterministic():
     assert float((lc - ls).abs().max()) <= LSE_TOL
     os2, ls2 = _gpu_fwd(qkv, 8, 128, "striped", True)
     assert torch.equal(os_, os2) and torch.equal(ls, ls2)
+    oz, lz = _gpu_fwd(qkv, 4, 128, "zigzag", True)
+    assert float((oz - os_).abs().max()) <= OUT_TOL
+    assert float((lz - ls).abs().max()) <= LSE_TOL
 
 
 def test_merge_entry_point_matches_oracle_merge():
