@@ -289,10 +289,11 @@ def run_ours(args, w, rank, world, local):
     peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
 
     # dominant kernel and its roofline (tensor-bound contraction)
+    hdrs = ("ra_internal.h", "ra_ptx.cuh", "ra_rows.cuh")     # included by both kernels
     if main_ms >= fwd_ms:
-        dom, dom_ms, dom_flops, files = "ra_bwd_kernel", main_ms, f_bwd, ("ra_bwd.cu",)
+        dom, dom_ms, dom_flops, files = "ra_bwd_kernel", main_ms, f_bwd, ("ra_bwd.cu",) + hdrs
     else:
-        dom, dom_ms, dom_flops, files = "ra_fwd_kernel", fwd_ms, f_fwd, ("ra_fwd.cu",)
+        dom, dom_ms, dom_flops, files = "ra_fwd_kernel", fwd_ms, f_fwd, ("ra_fwd.cu",) + hdrs
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
