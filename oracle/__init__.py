@@ -1,4 +1,4 @@
-"""CPU fp64 oracle for exact blockwise ring attention (contiguous and striped).
+"""CPU fp64 oracle for exact blockwise ring attention (contiguous, striped and zigzag).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import or run anything in this package.  The
@@ -25,6 +25,8 @@ Modules:
     ring      -- an fp64 emulator of the ring schedule with online softmax and the
                  partial merge, used only to test invariants ("ring == full").
     work      -- shard assignment, ring order and the per-shard work model.
+    gqa       -- grouped-query attention (fewer key/value heads than query heads) on top
+                 of ``attention``.
 
 Parity status: every function here is pinned by tests in ``tests/test_oracle_*.py``
 against things other than itself (a library softmax attention, closed forms,
@@ -36,9 +38,11 @@ from .attention import (attention_fwd, attention_bwd, attention_rows_fwd, attent
 from .ring import ring_fwd, ring_partials, merge_partials
 from .work import (shard_of, local_of, shard_tokens, ring_order, shard_work,
                    tile_class)
+from .gqa import gqa_fwd, gqa_bwd, group_size
 
 __all__ = [
     "attention_fwd", "attention_bwd", "attention_rows_fwd", "attention_rows_dq", "brute_force_fwd",
     "default_scale", "ring_fwd", "ring_partials", "merge_partials", "shard_of",
-    "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class",
+    "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class", "gqa_fwd", "gqa_bwd",
+    "group_size",
 ]
