@@ -6,7 +6,7 @@ then the backward's three stages (preprocess, main kernel, dQ finalize).  FLOPs 
 causal-useful work only: per unmasked (query, key) pair 4*D forward and 10*D backward
 (five products, the recompute included).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 32k|262k|1m|8k]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 32k|262k|1m|8k|32k-gqa]
                   [--layout striped|contiguous|zigzag] [--impl ours|reference]
 
 N > 1 runs under torchrun: every rank runs an independent replica on its own GPU (the
@@ -38,7 +38,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="32k", choices=["8k", "32k", "262k", "1m"])
+    ap.add_argument("--workload", default="32k", choices=["8k", "32k", "262k", "1m", "32k-gqa"])
     ap.add_argument("--layout", default=None, choices=["striped", "contiguous", "zigzag"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -80,7 +80,8 @@ def config_of(w):
     L, H, D = w["seq_len"], w["heads"], w["head_dim"]
     tensor_mib = w["batch"] * L * H * D * 2 / 2 ** 20
     return {"workload": "%s causal fwd+bwd, %s layout" % (w["name"], w["layout"]),
-            "batch": w["batch"], "heads": H, "head_dim": D, "seq_len": L, "P": w["P"],
+            "batch": w["batch"], "heads": H, "kv_heads": w.get("kv_heads", H),
+            "head_dim": D, "seq_len": L, "P": w["P"],
             "block": w["block"], "layout": w["layout"], "causal": w["causal"],
             "l2": "inputs larger than L2 (%.0f MiB per bf16 tensor, L2 129 MB)" % tensor_mib,
             "flops_per_step": sum(flops_of(w))}
@@ -232,7 +233,8 @@ def run_ours(args, w, rank, world, local):
     B, L, H, D, P, blk = (w["batch"], w["seq_len"], w["heads"], w["head_dim"], w["P"],
                           w["block"])
     layout, causal = w["layout"], w["causal"]
-    q, k, v, do = make_inputs(B, L, H, D, w["seed"] + 7919 * rank, device=dev)
+    q, k, v, do = make_inputs(B, L, H, D, w["seed"] + 7919 * rank, device=dev,
+                              kv_heads=w.get("kv_heads"))
     out = torch.empty_like(q)
     lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)

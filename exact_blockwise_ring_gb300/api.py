@@ -27,7 +27,8 @@ class Params(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("seq_len", ctypes.c_int64), ("heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("block", ctypes.c_int), ("P", ctypes.c_int),
                 ("layout", ctypes.c_int), ("causal", ctypes.c_int),
-                ("softmax_scale", ctypes.c_float), ("n_split", ctypes.c_int)]
+                ("softmax_scale", ctypes.c_float), ("n_split", ctypes.c_int),
+                ("kv_heads", ctypes.c_int)]
 
 
 class RaError(RuntimeError):
@@ -95,12 +96,12 @@ def _check(status):
 
 
 def make_params(batch, seq_len, heads, head_dim, P, block, layout="contiguous", causal=True,
-                softmax_scale=0.0, n_split=0):
+                softmax_scale=0.0, n_split=0, kv_heads=0):
     if isinstance(layout, str):
         layout = LAYOUTS[layout]
     return Params(int(batch), int(seq_len), int(heads), int(head_dim), int(block), int(P),
                   int(layout), int(bool(causal)) if isinstance(causal, bool) else int(causal),
-                  float(softmax_scale), int(n_split))
+                  float(softmax_scale), int(n_split), int(kv_heads))
 
 
 def _stream(stream):
@@ -112,15 +113,19 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _check_qkv(*ts):
-    shape = ts[0].shape
+def _check_qkv(q, k, v, dout=None):
+    """q (and dout) [B, L, H, D]; k, v [B, L, H_kv, D] with H_kv dividing H.  Returns
+    (B, L, H, D, H_kv)."""
+    ts = (q, k, v) if dout is None else (q, k, v, dout)
     for t in ts:
-        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != shape:
-            raise ValueError("q, k, v (and dout) must be contiguous CUDA bf16 tensors of one "
-                             "[B, L, H, D] shape")
-    if len(shape) != 4:
-        raise ValueError("expected [B, L, H, D]")
-    return shape
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v (and dout) must be contiguous 4-D CUDA bf16 tensors")
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    if (dout is not None and dout.shape != q.shape) or k.shape != v.shape or \
+            k.shape[:2] != (B, L) or k.shape[3] != D or Hkv < 1 or H % Hkv:
+        raise ValueError("expected q, dout [B, L, H, D] and k, v [B, L, H_kv, D], H_kv | H")
+    return B, L, H, D, Hkv
 
 
 class Workspace:
@@ -161,9 +166,10 @@ def bwd_workspace_bytes(params):
 def ra_fwd(q, k, v, P, block, layout="contiguous", causal=True, softmax_scale=0.0,
            out_dtype=torch.bfloat16, n_split=0, shard_work=False, workspace=None, stream=None,
            out=None, lse=None):
-    """Forward pass through ra_fwd.  Returns (out, lse) or (out, lse, shard_work[3, P])."""
-    B, L, H, D = _check_qkv(q, k, v)
-    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, n_split)
+    """Forward pass through ra_fwd.  Returns (out, lse) or (out, lse, shard_work[3, P]).
+    k and v may have fewer heads than q (grouped-query attention)."""
+    B, L, H, D, Hkv = _check_qkv(q, k, v)
+    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, n_split, Hkv)
     if out is None:
         out = torch.empty((B, L, H, D), dtype=out_dtype, device=q.device)
     if lse is None:
@@ -182,9 +188,9 @@ def ra_fwd(q, k, v, P, block, layout="contiguous", causal=True, softmax_scale=0.
 
 def ra_bwd(q, k, v, out, lse, dout, P, block, layout="contiguous", causal=True,
            softmax_scale=0.0, workspace=None, stream=None, dq=None, dk=None, dv=None):
-    """Backward pass through ra_bwd.  Returns (dq, dk, dv) bf16."""
-    B, L, H, D = _check_qkv(q, k, v, dout)
-    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, 0)
+    """Backward pass through ra_bwd.  Returns (dq, dk, dv) bf16, dk and dv shaped like k."""
+    B, L, H, D, Hkv = _check_qkv(q, k, v, dout)
+    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, 0, Hkv)
     odt = RA_FP32 if out.dtype == torch.float32 else RA_BF16
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -204,8 +210,8 @@ def ra_bwd_stages(q, k, v, out, lse, dout, dq, dk, dv, P, block, layout="contigu
 
     ``between(i)`` (optional) is called before stage i (0, 1, 2) and after the last
     (i = 3), e.g. to record CUDA events around each stage."""
-    B, L, H, D = _check_qkv(q, k, v, dout)
-    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, 0)
+    B, L, H, D, Hkv = _check_qkv(q, k, v, dout)
+    prm = make_params(B, L, H, D, P, block, layout, causal, softmax_scale, 0, Hkv)
     odt = RA_FP32 if out.dtype == torch.float32 else RA_BF16
     ws = workspace or default_workspace(q.device)
     buf = ws.get(max(bwd_workspace_bytes(prm), 256))

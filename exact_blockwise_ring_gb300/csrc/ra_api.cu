@@ -39,6 +39,9 @@ ra_status_t check_params(const ra_params_t* p, bool gpu_shapes) {
     return fail(RA_ERR_INVALID_ARG,
                 "layout must be RA_LAYOUT_CONTIGUOUS, RA_LAYOUT_STRIPED or RA_LAYOUT_ZIGZAG");
   if (p->causal != 0 && p->causal != 1) return fail(RA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (p->kv_heads < 0 || (p->kv_heads > 0 && p->heads % p->kv_heads != 0))
+    return fail(RA_ERR_INVALID_ARG, "kv_heads (%d) must be 0 or a divisor of heads (%d)",
+                p->kv_heads, p->heads);
   if (p->seq_len % p->P != 0 || (p->seq_len / p->P) % p->block != 0)
     return fail(RA_ERR_INVALID_ARG, "seq_len (%lld) must be divisible by P * block (%d * %d)",
                 (long long)p->seq_len, p->P, p->block);
@@ -63,6 +66,8 @@ ra_status_t check_params(const ra_params_t* p, bool gpu_shapes) {
   if (bhl > (1LL << 36)) return fail(RA_ERR_INVALID_ARG, "tensor too large");
   return RA_OK;
 }
+
+int kv_of(const ra_params_t* p) { return p->kv_heads > 0 ? p->kv_heads : p->heads; }
 
 float scale_of(const ra_params_t* p) {
   return p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)p->head_dim);
@@ -129,10 +134,12 @@ EncodeTiledFn encode_fn() {
 //   zigzag     dims (D, H, c, 2P, B): token = chunk * c + row, c = n / 2 (the kernels
 //              pick chunk = shard or 2P-1-shard from the local row)
 // (strides increase with the dimension index in every view).
-ra_status_t make_rows_map(CUtensorMap* m, const void* base, const ra_params_t* p, int box_rows) {
+// `heads` is the tensor's own head count (H for q, out, dout; H_kv for k, v).
+ra_status_t make_rows_map(CUtensorMap* m, const void* base, const ra_params_t* p, int heads,
+                          int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  const cuuint64_t D = p->head_dim, H = p->heads, P = p->P, B = p->batch;
+  const cuuint64_t D = p->head_dim, H = heads, P = p->P, B = p->batch;
   const cuuint64_t L = p->seq_len, n = L / P;
   cuuint64_t dims[5], strides[4];
   cuuint32_t box[5], es[5] = {1, 1, 1, 1, 1};
@@ -267,13 +274,14 @@ ra_status_t ra_fwd(const ra_params_t* p, const void* q, const void* k, const voi
                 workspace_bytes);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv;
-  if ((s = make_rows_map(&tq, q, p, kTile)) != RA_OK) return s;
-  if ((s = make_rows_map(&tk, k, p, kTile)) != RA_OK) return s;
-  if ((s = make_rows_map(&tv, v, p, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tq, q, p, p->heads, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tk, k, p, kv_of(p), kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tv, v, p, kv_of(p), kTile)) != RA_OK) return s;
 
   FwdArgs a{};
   a.B = p->batch;
   a.H = p->heads;
+  a.G = p->heads / kv_of(p);
   a.D = p->head_dim;
   a.P = p->P;
   a.layout = p->layout;
@@ -379,13 +387,15 @@ ra_status_t ra_bwd_main(const ra_params_t* p, const void* q, const void* k, cons
       !aligned16(dv))
     return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   CUtensorMap tq, tk, tv, tdo;
-  if ((s = make_rows_map(&tq, q, p, kTile)) != RA_OK) return s;
-  if ((s = make_rows_map(&tk, k, p, kTile)) != RA_OK) return s;
-  if ((s = make_rows_map(&tv, v, p, kTile)) != RA_OK) return s;
-  if ((s = make_rows_map(&tdo, dout, p, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tq, q, p, p->heads, kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tk, k, p, kv_of(p), kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tv, v, p, kv_of(p), kTile)) != RA_OK) return s;
+  if ((s = make_rows_map(&tdo, dout, p, p->heads, kTile)) != RA_OK) return s;
   BwdArgs a{};
   a.B = p->batch;
   a.H = p->heads;
+  a.Hkv = kv_of(p);
+  a.G = p->heads / a.Hkv;
   a.D = p->head_dim;
   a.P = p->P;
   a.layout = p->layout;

@@ -9,7 +9,10 @@
 // order (shard i = (j + k) mod P at step k for KV shard j), so dK and dV accumulate in
 // TMEM and leave once.  dQ partials are added into an fp32 accumulator in global memory.
 //
-// One CTA = 128 keys (tile u of shard j) of one (batch, head); query tiles of 128 rows.
+// One CTA = 128 keys (tile u of shard j) of one (batch, key/value head hk); query tiles of
+// 128 rows.  With grouped-query attention the G query heads h = hk*G + g that read this
+// key/value head pass one after another (g outermost, then the ring), so dK and dV sum
+// over the group in TMEM as they do over the ring.
 // Roles (640 threads):
 //   warp 0      producer: K, V once (TMA); per query tile Q, dO (TMA) and its 128 lse
 //               (log2 domain) and D values (bulk copies from the shard-major arrays the
@@ -159,8 +162,8 @@ __global__ void __launch_bounds__(640, 1)
     return;
   }
 
-  // ---- decode: one (batch, head) after another (the resident CTAs then share that
-  // head's Q, dO and dQ accumulator in L2); inside a head, heavy KV tiles first --------
+  // ---- decode: one (batch, key/value head) after another (the resident CTAs then share
+  // its query heads' Q, dO and dQ accumulator in L2); inside it, heavy KV tiles first ---
   const int per_bh = a.P * a.T;
   const int bh = blockIdx.x / per_bh;
   const int idx = blockIdx.x % per_bh;
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(640, 1)
     j = idx / a.T;
     u = idx % a.T;
   }
-  const int b = bh / a.H, h = bh % a.H;
+  const int b = bh / a.Hkv, hk = bh % a.Hkv;
   const BwdSched sc{j, u, a.n, a.T, a.P, a.layout, a.causal};
 
   if (threadIdx.x == 0) {
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const WaitCtx wc{abort_flag, a.err, a.wait_limit_ns};
-  const size_t ld_base = ((size_t)b * a.H + h) * a.L;   // [B, H, P, n] shard-major arrays
+  const size_t ld_base = (size_t)b * a.H * a.L;   // [B, H, P, n] shard-major arrays
 
   if (warp == 0) {
     // ================================================================ producer =====
@@ -216,28 +219,34 @@ __global__ void __launch_bounds__(640, 1)
       tma_prefetch_desc(&tmDO);
       mbar_expect_tx(kv_full, 2 * C::KB);
       for (int cb = 0; cb < 2; ++cb) {
-        load_rows(sK + cb * kTile * 128, &tmK, kv_full, a.layout, cb * 64, h, j, u * kTile, b,
+        load_rows(sK + cb * kTile * 128, &tmK, kv_full, a.layout, cb * 64, hk, j, u * kTile, b,
                   a.n, a.P);
-        load_rows(sV + cb * kTile * 128, &tmV, kv_full, a.layout, cb * 64, h, j, u * kTile, b,
+        load_rows(sV + cb * kTile * 128, &tmV, kv_full, a.layout, cb * 64, hk, j, u * kTile, b,
                   a.n, a.P);
       }
       int m = 0;
       bool ok = true;
-      for (int k = 0; k < a.P && ok; ++k) {
-        const int i = sc.i_of(k);
-        for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
-          const int st = m % NSTQ;
-          if (m >= NSTQ && !mbar_wait(&q_empty[st], ((m / NSTQ) - 1) & 1, wc)) { ok = false; break; }
-          mbar_expect_tx(&q_full[st], 2 * C::QB + C::LDB);
-          for (int cb = 0; cb < 2; ++cb) {
-            load_rows(sQ + st * C::QB + cb * BQ * 128, &tmQ, &q_full[st], a.layout, cb * 64, h, i,
-                      t * BQ, b, a.n, a.P);
-            load_rows(sDO + st * C::QB + cb * BQ * 128, &tmDO, &q_full[st], a.layout, cb * 64, h,
-                      i, t * BQ, b, a.n, a.P);
+      for (int g = 0; g < a.G && ok; ++g) {
+        const int h = hk * a.G + g;
+        for (int k = 0; k < a.P && ok; ++k) {
+          const int i = sc.i_of(k);
+          for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
+            const int st = m % NSTQ;
+            if (m >= NSTQ && !mbar_wait(&q_empty[st], ((m / NSTQ) - 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&q_full[st], 2 * C::QB + C::LDB);
+            for (int cb = 0; cb < 2; ++cb) {
+              load_rows(sQ + st * C::QB + cb * BQ * 128, &tmQ, &q_full[st], a.layout, cb * 64, h, i,
+                        t * BQ, b, a.n, a.P);
+              load_rows(sDO + st * C::QB + cb * BQ * 128, &tmDO, &q_full[st], a.layout, cb * 64, h,
+                        i, t * BQ, b, a.n, a.P);
+            }
+            const size_t off = ld_base + (size_t)h * a.L + (size_t)i * a.n + (size_t)t * BQ;
+            bulk_load(sLD + st * (2 * BQ), a.lse + off, BQ * 4, &q_full[st]);
+            bulk_load(sLD + st * (2 * BQ) + BQ, a.Dvec + off, BQ * 4, &q_full[st]);
           }
-          const size_t off = ld_base + (size_t)i * a.n + (size_t)t * BQ;
-          bulk_load(sLD + st * (2 * BQ), a.lse + off, BQ * 4, &q_full[st]);
-          bulk_load(sLD + st * (2 * BQ) + BQ, a.Dvec + off, BQ * 4, &q_full[st]);
         }
       }
       // let every copy this thread issued land before the CTA can exit
@@ -265,6 +274,7 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_after();
       int total = 0;
       for (int k = 0; k < a.P; ++k) total += sc.T - sc.t_lo(sc.i_of(k));
+      total *= a.G;
 
       // scores: A = K or V (K-major, 128 keys), B = Q or dO tile (K-major), K = D
 #define RA_SCORES(D_TM, AK, BADDR)                                                        \
@@ -346,78 +356,80 @@ __global__ void __launch_bounds__(640, 1)
     uint8_t* drow = sDS + half * (kTile * 128) + brow * 128;
     bool ok = true;
     int m = 0;
-    for (int k = 0; k < a.P && ok; ++k) {
-      const int i = sc.i_of(k);
-      for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
-        const int st = m % NSTQ;
-        if (!mbar_wait(s_full, m & 1, wc) || !mbar_wait(&q_full[st], (m / NSTQ) & 1, wc)) {
-          ok = false;
-          break;
-        }
-        // dS^T(m) overwrites the shared tile once dQ^T(m-1) and dK(m-1) have read it
-        if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        const float* lse2 = sLD + st * (2 * BQ) + 64 * half;   // -lse * log2(e)
-        const float* dvec = lse2 + BQ;                          // -D
-        const long long dl = a.causal ? sc.delta(i, t) : (1LL << 40);
-        // visible iff col - brow + delta >= 0 with col = 64*half + c, i.e. c >= lim
-        const long long lim = (long long)brow - dl - 64 * half;
-        // four passes of 16 query columns; pass p writes its P^T pairs to TMEM columns
-        // [64*half + 8p, +8), inside S^T columns this warpgroup has already read.
-        // Column pairs go through the packed fp32x2 FMA pipe: x = s*c + (-lse2),
-        // dS = P * (dP + (-D)); the mask is applied only on tiles that need one.
-        const bool masked = __any_sync(0xffffffffu, lim > 0);   // whole warp votes
-        const uint64_t c2 = f2_pack(sl2, sl2);
+    for (int g = 0; g < a.G && ok; ++g) {
+      for (int k = 0; k < a.P && ok; ++k) {
+        const int i = sc.i_of(k);
+        for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
+          const int st = m % NSTQ;
+          if (!mbar_wait(s_full, m & 1, wc) || !mbar_wait(&q_full[st], (m / NSTQ) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          // dS^T(m) overwrites the shared tile once dQ^T(m-1) and dK(m-1) have read it
+          if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          const float* lse2 = sLD + st * (2 * BQ) + 64 * half;   // -lse * log2(e)
+          const float* dvec = lse2 + BQ;                          // -D
+          const long long dl = a.causal ? sc.delta(i, t) : (1LL << 40);
+          // visible iff col - brow + delta >= 0 with col = 64*half + c, i.e. c >= lim
+          const long long lim = (long long)brow - dl - 64 * half;
+          // four passes of 16 query columns; pass p writes its P^T pairs to TMEM columns
+          // [64*half + 8p, +8), inside S^T columns this warpgroup has already read.
+          // Column pairs go through the packed fp32x2 FMA pipe: x = s*c + (-lse2),
+          // dS = P * (dP + (-D)); the mask is applied only on tiles that need one.
+          const bool masked = __any_sync(0xffffffffu, lim > 0);   // whole warp votes
+          const uint64_t c2 = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int pass = 0; pass < 4; ++pass) {
-          uint32_t sr[16], pr[16];
-          tmem_ld16(tS + 16 * pass, sr);
-          tmem_ld16(tDP + 16 * pass, pr);
-          tmem_wait_ld();
-          uint32_t pw[8], dw[8];
+          for (int pass = 0; pass < 4; ++pass) {
+            uint32_t sr[16], pr[16];
+            tmem_ld16(tS + 16 * pass, sr);
+            tmem_ld16(tDP + 16 * pass, pr);
+            tmem_wait_ld();
+            uint32_t pw[8], dw[8];
 #pragma unroll
-          for (int g8 = 0; g8 < 2; ++g8) {
-            const int cb = 16 * pass + 8 * g8;      // first of 8 columns
-            // negated lse2 and D of the 8 columns, as 4 packed pairs each
-            const ulonglong2 l01 = *reinterpret_cast<const ulonglong2*>(lse2 + cb);
-            const ulonglong2 l23 = *reinterpret_cast<const ulonglong2*>(lse2 + cb + 4);
-            const ulonglong2 d01 = *reinterpret_cast<const ulonglong2*>(dvec + cb);
-            const ulonglong2 d23 = *reinterpret_cast<const ulonglong2*>(dvec + cb + 4);
-            const uint64_t nl[4] = {l01.x, l01.y, l23.x, l23.y};
-            const uint64_t nd[4] = {d01.x, d01.y, d23.x, d23.y};
+            for (int g8 = 0; g8 < 2; ++g8) {
+              const int cb = 16 * pass + 8 * g8;      // first of 8 columns
+              // negated lse2 and D of the 8 columns, as 4 packed pairs each
+              const ulonglong2 l01 = *reinterpret_cast<const ulonglong2*>(lse2 + cb);
+              const ulonglong2 l23 = *reinterpret_cast<const ulonglong2*>(lse2 + cb + 4);
+              const ulonglong2 d01 = *reinterpret_cast<const ulonglong2*>(dvec + cb);
+              const ulonglong2 d23 = *reinterpret_cast<const ulonglong2*>(dvec + cb + 4);
+              const uint64_t nl[4] = {l01.x, l01.y, l23.x, l23.y};
+              const uint64_t nd[4] = {d01.x, d01.y, d23.x, d23.y};
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const int c = cb + 2 * e2;
-              const uint64_t s2 = f2_pack(__uint_as_float(sr[8 * g8 + 2 * e2]),
-                                          __uint_as_float(sr[8 * g8 + 2 * e2 + 1]));
-              const uint64_t dp2 = f2_pack(__uint_as_float(pr[8 * g8 + 2 * e2]),
-                                           __uint_as_float(pr[8 * g8 + 2 * e2 + 1]));
-              float x0, x1;
-              f2_unpack(f2_fma(s2, c2, nl[e2]), x0, x1);
-              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              if (masked) {
-                if ((long long)c < lim) p0 = 0.f;
-                if ((long long)c + 1 < lim) p1 = 0.f;
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int c = cb + 2 * e2;
+                const uint64_t s2 = f2_pack(__uint_as_float(sr[8 * g8 + 2 * e2]),
+                                            __uint_as_float(sr[8 * g8 + 2 * e2 + 1]));
+                const uint64_t dp2 = f2_pack(__uint_as_float(pr[8 * g8 + 2 * e2]),
+                                             __uint_as_float(pr[8 * g8 + 2 * e2 + 1]));
+                float x0, x1;
+                f2_unpack(f2_fma(s2, c2, nl[e2]), x0, x1);
+                float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                if (masked) {
+                  if ((long long)c < lim) p0 = 0.f;
+                  if ((long long)c + 1 < lim) p1 = 0.f;
+                }
+                const uint64_t pp2 = f2_pack(p0, p1);
+                float ds0, ds1;
+                f2_unpack(f2_mul(pp2, f2_add(dp2, nd[e2])), ds0, ds1);
+                pw[4 * g8 + e2] = pack_bf16x2(p0, p1);
+                dw[4 * g8 + e2] = pack_bf16x2(ds0, ds1);
               }
-              const uint64_t pp2 = f2_pack(p0, p1);
-              float ds0, ds1;
-              f2_unpack(f2_mul(pp2, f2_add(dp2, nd[e2])), ds0, ds1);
-              pw[4 * g8 + e2] = pack_bf16x2(p0, p1);
-              dw[4 * g8 + e2] = pack_bf16x2(ds0, ds1);
+            }
+            tmem_st8(tbase + lane_off + C::COL_S + 64 * half + 8 * pass, pw);
+#pragma unroll
+            for (int g8 = 0; g8 < 2; ++g8) {
+              const int c8 = 2 * pass + g8;           // 16-byte chunk inside the 128-byte row
+              *reinterpret_cast<uint4*>(drow + ((c8 ^ (brow & 7)) * 16)) =
+                  make_uint4(dw[4 * g8], dw[4 * g8 + 1], dw[4 * g8 + 2], dw[4 * g8 + 3]);
             }
           }
-          tmem_st8(tbase + lane_off + C::COL_S + 64 * half + 8 * pass, pw);
-#pragma unroll
-          for (int g8 = 0; g8 < 2; ++g8) {
-            const int c8 = 2 * pass + g8;           // 16-byte chunk inside the 128-byte row
-            *reinterpret_cast<uint4*>(drow + ((c8 ^ (brow & 7)) * 16)) =
-                make_uint4(dw[4 * g8], dw[4 * g8 + 1], dw[4 * g8 + 2], dw[4 * g8 + 3]);
-          }
+          fence_proxy_async_smem();
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(ds_ready);
         }
-        fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(ds_ready);
       }
     }
     // ---- dK, dV epilogue (thread = key row): warpgroup 0 writes dV, 1 writes dK ------
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_after();
       const int loc = u * kTile + brow;
       const long long tok = token_of(a.layout, j, loc, a.n, a.P);
-      const size_t row = ((size_t)b * a.L + tok) * a.H + h;
+      const size_t row = ((size_t)b * a.L + tok) * a.Hkv + hk;
       const bool any = m > 0;
       const uint32_t tcol = tbase + lane_off + (half ? C::COL_DK : C::COL_DV);
       const float mul = half ? a.scale : 1.f;
@@ -453,29 +465,32 @@ __global__ void __launch_bounds__(640, 1)
     const int half = (warp - 12) >> 2;
     const int drow = wq * 32 + lane;
     const uint32_t tQ = tbase + (static_cast<uint32_t>(wq * 32) << 16) + C::COL_DP + 64 * half;
-    float* dq_head = a.dq_acc + (size_t)b * a.L * a.H * D_ + (size_t)h * D_ + drow;
     const long long qstride = (a.layout == RA_LAYOUT_STRIPED) ? (long long)a.P * a.H * D_
                                                               : (long long)a.H * D_;
     bool ok = true;
     int m = 0;
-    for (int k = 0; k < a.P && ok; ++k) {
-      const int i = sc.i_of(k);
-      for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
-        if (!mbar_wait(dq_full, m & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t q0[32], q1[32];
-        tmem_ld32(tQ, q0);
-        tmem_ld32(tQ + 32, q1);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        // 64 consecutive local rows: consecutive tokens (stride qstride) in every layout
-        const long long tok0 = token_of(a.layout, i, t * BQ + 64 * half, a.n, a.P);
-        float* p0 = dq_head + tok0 * a.H * D_;
+    for (int g = 0; g < a.G && ok; ++g) {
+      float* dq_head =
+          a.dq_acc + (size_t)b * a.L * a.H * D_ + (size_t)(hk * a.G + g) * D_ + drow;
+      for (int k = 0; k < a.P && ok; ++k) {
+        const int i = sc.i_of(k);
+        for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
+          if (!mbar_wait(dq_full, m & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t q0[32], q1[32];
+          tmem_ld32(tQ, q0);
+          tmem_ld32(tQ + 32, q1);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(dq_empty);
+          // 64 consecutive local rows: consecutive tokens (stride qstride) in every layout
+          const long long tok0 = token_of(a.layout, i, t * BQ + 64 * half, a.n, a.P);
+          float* p0 = dq_head + tok0 * a.H * D_;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * qstride, __uint_as_float(q0[c]));
+          for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * qstride, __uint_as_float(q0[c]));
 #pragma unroll
-        for (int c = 0; c < 32; ++c) red_add_f32(p0 + (32 + c) * qstride, __uint_as_float(q1[c]));
+          for (int c = 0; c < 32; ++c) red_add_f32(p0 + (32 + c) * qstride, __uint_as_float(q1[c]));
+        }
       }
     }
   }
@@ -496,7 +511,7 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(ra_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BwdCfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)a.B * a.H * a.P * a.T;
+  const long long grid = (long long)a.B * a.Hkv * a.P * a.T;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   ra_bwd_kernel<<<(unsigned)grid, 640, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();

@@ -11,7 +11,9 @@
 //     are skipped, the diagonal tile is masked, earlier tiles are not.
 //
 // One CTA owns 256 query rows of one (batch, head, shard): two 128-row tiles that share
-// every K/V tile loaded.  Roles (384 threads):
+// every K/V tile loaded.  With grouped-query attention query head h reads key/value head
+// h / G; CTAs run head after head, so the G query heads of a group, which read the same
+// K/V, are adjacent in launch order and share those tiles in L2.  Roles (384 threads):
 //   warp 0      TMA producer of Q (once) and of the K tiles (NK-stage ring)
 //   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
 //   warp 2      per-shard work counter (one thread), otherwise idle
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(384, 1)
     i = idx % a.P;
   }
   const int b = bh / a.H, h = bh % a.H;
+  const int hkv = h / a.G;        // key/value head of this query head
   const int steps = a.P / a.n_split;
   RingSched sc{i, 2 * s, 2, a.T, a.P, a.layout, a.causal, g * steps, (g + 1) * steps};
   const int nvalid = (2 * s + 1 < a.T) ? 2 : 1;
@@ -234,8 +237,8 @@ __global__ void __launch_bounds__(384, 1)
           if (n >= NS && !mbar_wait(&empty[st], ((n / NS) - 1) & 1, wc)) { ok = false; break; }
           mbar_expect_tx(&full[st], C::KVB);
           for (int cb = 0; cb < C::NCB; ++cb)
-            load_rows(ring + st * C::KVB + cb * kTile * 128, tm, &full[st], a.layout, cb * 64, h,
-                      j, u * kTile, b, a.n, a.P);
+            load_rows(ring + st * C::KVB + cb * kTile * 128, tm, &full[st], a.layout, cb * 64,
+                      hkv, j, u * kTile, b, a.n, a.P);
         }
       }
       // let every copy this thread issued land before the CTA can exit
@@ -286,7 +289,8 @@ __global__ void __launch_bounds__(384, 1)
       int n = 0;
       for (int k = sc.k0; k < sc.k1 && ok; ++k) {
         const int j = sc.j_of(k);
-        const int ue = sc.u_end(j);
+        const int ue0 = sc.q_end(0, j), ue1 = sc.q_end(1, j);
+        const int ue = ue0 > ue1 ? ue0 : ue1;
         for (int u = 0; u < ue; ++u, ++n) {
           const int kst = n % NK, vst = n % NV;
           if (!mbar_wait(&k_full[kst], (n / NK) & 1, wc)) { ok = false; break; }
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(384, 1)
           // query tile 0
           if (pend0 >= 0) RA_ISSUE_PV(pend0, ppar0, pv0, &p_full[0], dO0, dS0);
           if (!ok) break;
-          if (sc.cls(0, j, u) != kSkip) {
+          if (u < ue0) {
             RA_ISSUE_S(q0d, dS0);
             umma_commit(&s_full[0]);
             pend0 = vst;
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(384, 1)
           // query tile 1
           if (pend1 >= 0) RA_ISSUE_PV(pend1, ppar1, pv1, &p_full[1], dO1, dS1);
           if (!ok) break;
-          if (sc.cls(1, j, u) != kSkip) {
+          if (u < ue1) {
             RA_ISSUE_S(q1d, dS1);
             umma_commit(&s_full[1]);
             pend1 = vst;
@@ -344,10 +348,8 @@ __global__ void __launch_bounds__(384, 1)
     if (valid) {
       for (int k = sc.k0; k < sc.k1 && ok; ++k) {
         const int j = sc.j_of(k);
-        const int ue = sc.u_end(j);
-        for (int u = 0; u < ue; ++u) {
-          const int cl = sc.cls(q, j, u);
-          if (cl == kSkip) continue;
+        const int ueq = sc.q_end(q, j), udiag = sc.q_diag(q, j);
+        for (int u = 0; u < ueq; ++u) {
           if (!mbar_wait(&s_full[q], cnt & 1, wc)) { ok = false; break; }
           tc_fence_after();
           float sv[128];
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(r[e]);
           }
-          if (cl == kDiag) {
+          if (u == udiag) {
             const int lim = arow - ((a.layout == RA_LAYOUT_STRIPED && j > i) ? 1 : 0);
 #pragma unroll
             for (int e = 0; e < 128; ++e)

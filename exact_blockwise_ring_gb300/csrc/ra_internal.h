@@ -19,8 +19,6 @@ constexpr int kAutoSplitSMs = 152;
 // Default limit for every in-kernel wait.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-enum TileClass : int { kSkip = 0, kFull = 1, kDiag = 2 };
-
 // ---- token assignment (n = L / P tokens per shard) ----------------------------------
 //   contiguous: local row a of shard i is token i*n + a
 //   striped:    token a*P + i
@@ -95,7 +93,9 @@ __host__ __device__ inline long long tokens_upto(int layout, int j, long long to
 //               gk = block_pos(j, u); skip gk > gq, diag gk == gq (mask b <= a);
 //   striped:    skip u > t, diag u == t (mask inside: key b visible to query a iff
 //               b < a, or b == a and j <= i), full u < t.
-// In every layout the visible KV tiles of a shard form a prefix u < u_end(j).
+// In every layout the KV tiles of shard j that query tile t0+q sees form a prefix
+// u < q_end(q, j), of which only the last can be the diagonal one (q_diag, -1 if none);
+// u_end(j) is the longest such prefix over the unit's query tiles.
 struct RingSched {
   int i, t0, nq, T, P, layout, causal, k0, k1;
 
@@ -103,25 +103,34 @@ struct RingSched {
     int j = (i - k) % P;
     return j < 0 ? j + P : j;
   }
-  __host__ __device__ int u_end(int j) const {
-    if (!causal) return T;
-    int tmax = t0 + nq - 1;
-    if (tmax > T - 1) tmax = T - 1;
-    if (layout == RA_LAYOUT_STRIPED) return tmax + 1;
-    return (int)blocks_upto(layout, j, block_pos(layout, i, tmax, T, P), T, P);
-  }
-  __host__ __device__ int cls(int q, int j, int u) const {
+  __host__ __device__ int q_end(int q, int j) const {
     const int t = t0 + q;
-    if (q >= nq || t >= T) return kSkip;
-    if (!causal) return kFull;
-    if (layout == RA_LAYOUT_STRIPED) return u < t ? kFull : (u == t ? kDiag : kSkip);
-    const long long gq = block_pos(layout, i, t, T, P), gk = block_pos(layout, j, u, T, P);
-    return gk < gq ? kFull : (gk == gq ? kDiag : kSkip);
+    if (q >= nq || t >= T) return 0;
+    if (!causal) return T;
+    if (layout == RA_LAYOUT_STRIPED) return t + 1;
+    return (int)blocks_upto(layout, j, block_pos(layout, i, t, T, P), T, P);
+  }
+  __host__ __device__ int q_diag(int q, int j) const {
+    const int t = t0 + q;
+    if (!causal || q >= nq || t >= T) return -1;
+    if (layout == RA_LAYOUT_STRIPED) return t;
+    const int e = q_end(q, j);
+    return (e > 0 && block_pos(layout, j, e - 1, T, P) == block_pos(layout, i, t, T, P)) ? e - 1
+                                                                                        : -1;
+  }
+  __host__ __device__ int u_end(int j) const {
+    int e = 0;
+    for (int q = 0; q < nq; ++q) {
+      const int x = q_end(q, j);
+      e = x > e ? x : e;
+    }
+    return e;
   }
 };
 
 struct FwdArgs {
   int B, H, D, P, layout, causal, block;
+  int G;          // query heads per key/value head: query head h reads K/V head h / G
   int64_t L;
   int n;          // tokens per shard, L / P
   int T;          // 128-row tiles per shard
@@ -140,6 +149,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   int B, H, D, P, layout, causal;
+  int Hkv, G;     // key/value heads; query heads per key/value head (h = hk * G + g)
   int64_t L;
   int n, T;
   float scale;        // softmax scale

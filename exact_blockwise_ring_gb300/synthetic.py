@@ -20,13 +20,18 @@ WORKLOADS = {
                   causal=True, layouts=("striped", "zigzag"), backward=True),
     "1m":    dict(batch=1, heads=8, head_dim=128, seq_len=1048576, P=32, block=256,
                   causal=True, layouts=("striped", "contiguous", "zigzag"), backward=True),
+    # grouped-query attention: 32 query heads on 8 key/value heads (4 per group)
+    "32k-gqa": dict(batch=1, heads=32, kv_heads=8, head_dim=128, seq_len=32768, P=8,
+                    block=128, causal=True, layouts=("zigzag", "striped"), backward=True),
 }
 
-SEEDS = {"tiny": 1000, "8k": 1001, "32k": 1002, "262k": 1003, "1m": 1004}
+SEEDS = {"tiny": 1000, "8k": 1001, "32k": 1002, "262k": 1003, "1m": 1004, "32k-gqa": 1005}
 
 
-def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=True):
-    """Return (q, k, v[, dout]) bfloat16 tensors [B, L, H, D] on ``device``.
+def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=True,
+                kv_heads=None):
+    """Return (q, k, v[, dout]) bfloat16 tensors on ``device``: q and dout
+    [B, L, heads, D], k and v [B, L, kv_heads, D] (kv_heads defaults to heads).
 
     The generator lives on ``device``; CPU and CUDA streams of numbers differ, so
     a test that compares against the oracle generates on the CPU (or copies device
@@ -34,11 +39,14 @@ def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=T
     """
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
-    shape = (batch, seq_len, heads, head_dim)
+    hq = heads
+    hkv = heads if kv_heads is None else kv_heads
     names = ("q", "k", "v", "dout") if with_dout else ("q", "k", "v")
     out = []
-    for _ in names:
-        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    for nm in names:
+        h = hkv if nm in ("k", "v") else hq
+        x = torch.randn((batch, seq_len, h, head_dim), generator=g, device=device,
+                        dtype=torch.float32)
         out.append(x.to(torch.bfloat16))
     return tuple(out)
 

@@ -19,7 +19,8 @@
  * one kernel, and a "hop" is a tile load of KV shard (i - k) mod P from device memory.
  *
  * Conventions for every entry point:
- *   - Tensors are row-major.  q, k, v, out, dout, dq, dk, dv are [B, L, H, D] with
+ *   - Tensors are row-major.  q, out, dout, dq are [B, L, H, D] and k, v, dk, dv are
+ *     [B, L, H_kv, D] (H_kv = H unless kv_heads says otherwise), with
  *     tokens in NATURAL order for every layout (the shard permutation is internal;
  *     attention is permutation-equivariant, aibr.jp Striped Attention summary, §3).
  *     lse is float32 [B, H, L], natural logarithm.
@@ -81,6 +82,12 @@ typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype_t;
  *                    ring steps; g > 1 (g divides P) = the ring steps are cut into g
  *                    groups, each writing a partial (O_g, lse_g) that ra_merge then
  *                    combines; 0 = let the library choose.
+ *   kv_heads         H_kv, the number of key/value heads: 0 (or H) for plain multi-head
+ *                    attention, otherwise a divisor of H (grouped-query attention; 1 is
+ *                    MQA).  Query head h attends with key/value head h / (H / H_kv), i.e.
+ *                    G = H / H_kv consecutive query heads share one; the gradient of a
+ *                    shared head is the sum over its G query heads (labhub, comparison
+ *                    section "比較分析": ring attention is fully compatible with GQA/MQA).
  */
 typedef struct {
   int batch;
@@ -93,6 +100,7 @@ typedef struct {
   int causal;
   float softmax_scale;
   int n_split;
+  int kv_heads;
 } ra_params_t;
 
 /* Bytes of device workspace ra_fwd / ra_bwd need for `p` (0 if `p` is invalid).

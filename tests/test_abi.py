@@ -36,11 +36,11 @@ def test_status_strings(L):
 
 def _params(**kw):
     base = dict(batch=1, seq_len=1024, heads=2, head_dim=128, P=4, block=128, layout=0,
-                causal=1, softmax_scale=0.0, n_split=0)
+                causal=1, softmax_scale=0.0, n_split=0, kv_heads=0)
     base.update(kw)
     return api.Params(base["batch"], base["seq_len"], base["heads"], base["head_dim"],
                       base["block"], base["P"], base["layout"], base["causal"],
-                      base["softmax_scale"], base["n_split"])
+                      base["softmax_scale"], base["n_split"], base["kv_heads"])
 
 
 FAKE = ctypes.c_void_p(1 << 20)      # 16-byte aligned, never dereferenced on these paths
@@ -64,6 +64,8 @@ def _fwd(L, prm, q=FAKE, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30, odt=0, s
     (dict(softmax_scale=-1.0), 1),
     (dict(softmax_scale=float("inf")), 1),
     (dict(n_split=3), 1),                 # not a divisor of P
+    (dict(heads=6, kv_heads=4), 1),       # kv_heads must divide heads
+    (dict(kv_heads=-1), 1),
 ])
 def test_fwd_rejects_bad_params(L, kw, code):
     assert _fwd(L, _params(**kw)) == code

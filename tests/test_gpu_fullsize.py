@@ -29,7 +29,7 @@ def _rows(L, P, layout):
 
 
 CASES = [("32k", "striped"), ("262k", "striped"), ("1m", "striped"), ("1m", "contiguous"),
-         ("32k", "zigzag"), ("1m", "zigzag")]
+         ("32k", "zigzag"), ("1m", "zigzag"), ("32k-gqa", "zigzag")]
 
 
 @pytest.mark.parametrize("name,layout", CASES)
@@ -37,8 +37,10 @@ def test_fullsize_parity(name, layout):
     w = WORKLOADS[name]
     B, L, H, D, P, blk = (w["batch"], w["seq_len"], w["heads"], w["head_dim"], w["P"],
                           w["block"])
+    Hkv = w.get("kv_heads", H)
+    G = H // Hkv
     dev = torch.device("cuda:0")
-    q, k, v, do = make_inputs(B, L, H, D, SEEDS[name], device=dev)
+    q, k, v, do = make_inputs(B, L, H, D, SEEDS[name], device=dev, kv_heads=Hkv)
     out, lse = era.ra_fwd(q, k, v, P, blk, layout, True)               # as the bench runs it
     dq, dk, dv = era.ra_bwd(q, k, v, out, lse, do, P, blk, layout, True)
     o32, l32 = era.ra_fwd(q, k, v, P, blk, layout, True, out_dtype=torch.float32)
@@ -47,8 +49,8 @@ def test_fullsize_parity(name, layout):
     rows = _rows(L, P, layout)
     for h in sorted({0, H - 1}):
         # one head on the host in float64 (only its keys/values are needed)
-        qh, kh, vh, doh = (t[0, :, h, :].double().cpu().numpy()[None, :, None, :]
-                           for t in (q, k, v, do))
+        qh, doh = (t[0, :, h, :].double().cpu().numpy()[None, :, None, :] for t in (q, do))
+        kh, vh = (t[0, :, h // G, :].double().cpu().numpy()[None, :, None, :] for t in (k, v))
         ro, rl = oracle.attention_rows_fwd(qh, kh, vh, 0, 0, rows, causal=True)
         go = o32[0, rows, h, :].double().cpu().numpy()
         gl = l32[0, h, rows].double().cpu().numpy()
@@ -69,6 +71,6 @@ def test_fullsize_parity(name, layout):
     sk = dk.double().sum(dim=1)
     assert float(sk.norm() / dk.double().norm()) <= GRAD_TOL
     sv = dv.double().sum(dim=1)
-    so = do.double().sum(dim=1)
+    so = do.double().sum(dim=1).view(B, Hkv, G, D).sum(2)      # query heads of each group
     assert float((sv - so).norm() / so.norm()) <= GRAD_TOL
     assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
