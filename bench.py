@@ -42,6 +42,7 @@ def parse_args():
     ap.add_argument("--layout", default=None, choices=["striped", "contiguous", "zigzag"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-merge", action="store_true")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     return a
@@ -222,6 +223,37 @@ def traffic_for(kernel, src_files):
     return None
 
 
+def hbm_line(nbytes, ms, peak_gbs):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"bytes": int(nbytes), "ms": round(ms, 4), "achieved_gbs": round(gbs, 1),
+            "frac": round(gbs / peak_gbs, 4)}
+
+
+def time_merge(era, B, L, H, D, dev, stream, peak_gbs, n_parts=4, reps=5):
+    """ra_merge on n_parts fp32 partials [n, B, L, H, D] (inputs larger than L2), CUDA
+    events on the launching stream; algorithmic bytes = partials and their lse read once,
+    bf16 output and lse written once."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    o_parts = torch.randn((n_parts, B, L, H, D), generator=g, device=dev, dtype=torch.float32)
+    lse_parts = torch.randn((n_parts, B, H, L), generator=g, device=dev, dtype=torch.float32)
+    for _ in range(2):
+        era.ra_merge(o_parts, lse_parts, stream=stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        era.ra_merge(o_parts, lse_parts, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    rows = B * L * H
+    nbytes = n_parts * rows * (4 * D + 4) + rows * (2 * D + 4)
+    line = hbm_line(nbytes, e0.elapsed_time(e1) / reps, peak_gbs)
+    line["n_parts"] = n_parts
+    return line
+
+
 # ---------------------------------------------------------------- our arm ----------
 def run_ours(args, w, rank, world, local):
     import torch
@@ -335,6 +367,21 @@ def run_ours(args, w, rank, world, local):
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e_ms / K, 3)}
 
+    # the bandwidth-bound kernels against the measured HBM copy rate: the backward's
+    # preprocess and finalize (timed inside the steps above) and the partial merge (timed
+    # here, after the steps, on 4 fp32 partials of the workload's shape)
+    hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    rows = B * L * H
+    pre_bytes = rows * (2 * D + out.element_size() * D + 4 + 8 + 4 * D)
+    fin_bytes = rows * D * (4 + 2)
+    hbm_kernels = {
+        "peak_gbs": hbm, "peak_kind": "hbm_gbs of %s" % pk_kind,
+        "bwd_pre_kernel": hbm_line(pre_bytes, pre_ms, hbm),
+        "dq_convert_kernel": hbm_line(fin_bytes, fin_ms, hbm),
+    }
+    if not args.no_merge:
+        hbm_kernels["merge_kernel"] = time_merge(era, B, L, H, D, dev, stream, hbm)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
@@ -348,7 +395,8 @@ def run_ours(args, w, rank, world, local):
                 "config": config_of(w),
                 "stage_ms": {"fwd": round(fwd_ms, 3), "bwd_preprocess": round(pre_ms, 3),
                              "bwd_main": round(main_ms, 3), "bwd_finalize": round(fin_ms, 3)},
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "hbm_kernels": hbm_kernels, "cpu_baseline": cpu,
+                "e2e": e2e,
                 "gpu_launches": 4 * K, "clocks": clk}
         print(json.dumps(line), flush=True)
 

@@ -1,4 +1,5 @@
-"""Exact blockwise ring attention (contiguous and striped) for NVIDIA GB300 (sm_103a).
+"""Exact blockwise ring attention (contiguous, striped and zigzag layouts; multi-head or
+grouped-query) for NVIDIA GB300 (sm_103a).
 
 The computation lives in libra.so (C ABI: include/ra.h), built from csrc/ by
 ``exact_blockwise_ring_gb300.build.build()``; this package only marshals arguments.

@@ -368,11 +368,11 @@ ra_status_t ra_bwd_preprocess(const ra_params_t* p, const void* out, int out_dty
   if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
     return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_bwd_pre(out, out_dtype == RA_FP32, dout, lse, w.Dsm, w.L2sm, p->batch,
-                                 p->seq_len, p->heads, p->head_dim, p->P, p->layout, st);
+  // one kernel: D, lse * log2(e) (shard-major, negated) and the zeroed dQ accumulator
+  cudaError_t e = launch_bwd_pre(out, out_dtype == RA_FP32, dout, lse, w.Dsm, w.L2sm, w.dq_acc,
+                                 p->batch, p->seq_len, p->heads, p->head_dim, p->P, p->layout,
+                                 st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
-  e = cudaMemsetAsync(w.dq_acc, 0, w.o * 4, st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dq accumulator)");
   return RA_OK;
 }
 

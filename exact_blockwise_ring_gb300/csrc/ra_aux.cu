@@ -26,16 +26,21 @@ __device__ __forceinline__ void store4(void* out, int out_fp32, size_t elem, flo
   }
 }
 
-// One warp per output row (b, token, h); each lane owns 4 consecutive features per
-// 128-feature chunk.  Weights exp(lse_g - max) are computed by every lane (n is small).
+// Merge of n_parts normalised partials.  A row (b, token, h) is handled by `lpr` lanes
+// (D/8 rounded up to a power of two), each owning 8 consecutive features.  The partial
+// outputs of the first kPrefetch parts are loaded before the lse pass, so that their DRAM
+// latency overlaps the lse loads instead of following them; further parts stream after.
+constexpr int kPrefetch = 4;
+
 __global__ void __launch_bounds__(256)
     merge_kernel(int n_parts, const float* __restrict__ o_parts,
-                 const float* __restrict__ lse_parts, int B, long long L, int H, int D,
+                 const float* __restrict__ lse_parts, int B, long long L, int H, int D, int lpr,
                  void* out, int out_fp32, float* lse) {
   const long long rows = (long long)B * L * H;
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / lpr;
+  const int sub = threadIdx.x % lpr;
   if (row >= rows) return;
-  const int lane = threadIdx.x & 31;
+  const bool act = 8 * sub < D;
   const int h = (int)(row % H);
   const long long bl = row / H;
   const long long tok = bl % L;
@@ -43,69 +48,109 @@ __global__ void __launch_bounds__(256)
   const size_t lidx = ((size_t)b * H + h) * L + tok;
   const size_t part_o = (size_t)rows * D;
   const size_t part_l = (size_t)B * H * L;
+  const size_t e = (size_t)row * D + 8 * sub;
+  float4 pa[kPrefetch], pb[kPrefetch];
+#pragma unroll
+  for (int g = 0; g < kPrefetch; ++g) {
+    if (act && g < n_parts) {
+      const float4* src = reinterpret_cast<const float4*>(o_parts + g * part_o + e);
+      pa[g] = __ldg(src);
+      pb[g] = __ldg(src + 1);
+    } else {
+      pa[g] = pb[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   float mx = kNegInf;
-  for (int g = 0; g < n_parts; ++g) mx = fmaxf(mx, lse_parts[g * part_l + lidx]);
+  for (int g = 0; g < n_parts; ++g) mx = fmaxf(mx, __ldg(lse_parts + g * part_l + lidx));
   float tot = 0.f;
   if (mx != kNegInf)
     for (int g = 0; g < n_parts; ++g) {
-      const float l = lse_parts[g * part_l + lidx];
+      const float l = __ldg(lse_parts + g * part_l + lidx);
       if (l != kNegInf) tot += expf(l - mx);
     }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  for (int d0 = lane * 4; d0 < D; d0 += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (tot > 0.f)
-      for (int g = 0; g < n_parts; ++g) {
-        const float l = lse_parts[g * part_l + lidx];
+  if (act) {
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    if (tot > 0.f) {
+      // prefetched parts (static register indices), then the rest streamed
+#pragma unroll
+      for (int g = 0; g < kPrefetch; ++g) {
+        if (g >= n_parts) break;
+        const float l = __ldg(lse_parts + g * part_l + lidx);
+        if (l == kNegInf) continue;       // skipped, whatever its partial holds
+        const float w = expf(l - mx) * inv;
+        a0.x += w * pa[g].x; a0.y += w * pa[g].y; a0.z += w * pa[g].z; a0.w += w * pa[g].w;
+        a1.x += w * pb[g].x; a1.y += w * pb[g].y; a1.z += w * pb[g].z; a1.w += w * pb[g].w;
+      }
+      for (int g = kPrefetch; g < n_parts; ++g) {
+        const float l = __ldg(lse_parts + g * part_l + lidx);
         if (l == kNegInf) continue;
         const float w = expf(l - mx) * inv;
-        const float4 o = __ldg(reinterpret_cast<const float4*>(o_parts + g * part_o +
-                                                                (size_t)row * D + d0));
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+        const float4* src = reinterpret_cast<const float4*>(o_parts + g * part_o + e);
+        const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+        a0.x += w * x0.x; a0.y += w * x0.y; a0.z += w * x0.z; a0.w += w * x0.w;
+        a1.x += w * x1.x; a1.y += w * x1.y; a1.z += w * x1.z; a1.w += w * x1.w;
       }
-    store4(out, out_fp32, (size_t)row * D + d0, acc);
+    }
+    store4(out, out_fp32, e, a0);
+    store4(out, out_fp32, e + 4, a1);
   }
-  if (lane == 0) lse[lidx] = tot > 0.f ? mx + logf(tot) : kNegInf;
+  if (sub == 0) lse[lidx] = tot > 0.f ? mx + logf(tot) : kNegInf;
 }
 
-// Backward preprocess, one warp per row (b, token, h):
+// Backward preprocess.  Per row (b, token, h):
 //   nD[b, h, shard, local]    = -sum_d dO[b, token, h, d] * O[b, token, h, d]
 //   nlse2[b, h, shard, local] = -lse[b, h, token] * log2(e)
-// written shard-major so the values of one query tile are one contiguous block, and
-// negated so that the backward's s*c - lse2 and dP - D are single packed FMAs/adds.
+//   dq_acc[b, token, h, :]    = 0          (the backward main kernel adds into it)
+// nD and nlse2 are written shard-major so the values of one query tile are one contiguous
+// block, and negated so that the backward's s*c - lse2 and dP - D are single packed
+// FMAs/adds.  A row is handled by D/8 consecutive lanes (8 features each: one 16-byte
+// load of dO, one or two of O, two 16-byte stores of zeros), so a warp covers 256/D rows
+// per pass; the dot product is reduced with shuffles inside each lane group.
 __global__ void __launch_bounds__(256)
     bwd_pre_kernel(const void* __restrict__ out, int out_fp32, const __nv_bfloat16* __restrict__ dout,
                    const float* __restrict__ lse, float* __restrict__ Dsm, float* __restrict__ L2sm,
-                   int B, long long L, int H, int D, int P, int layout) {
+                   float* __restrict__ dq_acc, int B, long long L, int H, int D, int P,
+                   int layout) {
+  const int lpr = D >> 3;                             // lanes per row (8 or 16)
   const long long rows = (long long)B * L * H;
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const int lane = threadIdx.x & 31;
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / lpr;
+  const int sub = threadIdx.x % lpr;
+  const bool live = row < rows;
   float acc = 0.f;
-  for (int d0 = lane * 4; d0 < D; d0 += 128) {
-    const size_t e = (size_t)row * D + d0;
-    const uint2 gw = __ldg(reinterpret_cast<const uint2*>(dout + e));
-    const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
-    const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
-    float4 o;
+  if (live) {
+    const size_t e = (size_t)row * D + 8 * sub;
+    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(dout + e));
+    float o[8];
     if (out_fp32) {
-      o = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(out) + e));
+      const float4 a = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(out) + e));
+      const float4 c = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(out) + e) + 1);
+      o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+      o[4] = c.x; o[5] = c.y; o[6] = c.z; o[7] = c.w;
     } else {
-      const uint2 ow = __ldg(reinterpret_cast<const uint2*>(
+      const uint4 ow = __ldg(reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(out) + e));
-      const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow.x));
-      const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow.y));
-      o = make_float4(o01.x, o01.y, o23.x, o23.y);
-    }
-    const float2 g0 = __bfloat1622float2(g01), g1 = __bfloat1622float2(g23);
-    acc += g0.x * o.x + g0.y * o.y + g1.x * o.z + g1.y * o.w;
-  }
+      const uint32_t ov[4] = {ow.x, ow.y, ow.z, ow.w};
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
+      for (int x = 0; x < 4; ++x) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[x]));
+        o[2 * x] = f.x;
+        o[2 * x + 1] = f.y;
+      }
+    }
+    const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[x]));
+      acc += g.x * o[2 * x] + g.y * o[2 * x + 1];
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + e);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // lane groups are aligned to lpr (a power of two dividing 32): xor stays inside a group
+  for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (live && sub == 0) {
     const int h = (int)(row % H);
     const long long bl = row / H;
     const long long tok = bl % L;
@@ -165,19 +210,23 @@ unsigned grid_for(long long rows, int rows_per_block) {
 cudaError_t launch_merge(int n_parts, const float* o_parts, const float* lse_parts, int B,
                          int64_t L, int H, int D, void* out, int out_fp32, float* lse,
                          cudaStream_t s) {
+  if (D % 8 != 0 || D < 8 || D > 256) return cudaErrorInvalidValue;
   const long long rows = (long long)B * L * H;
-  merge_kernel<<<grid_for(rows, 8), 256, 0, s>>>(n_parts, o_parts, lse_parts, B, L, H, D, out,
-                                                 out_fp32, lse);
+  int lpr = 1;
+  while (lpr < D / 8) lpr <<= 1;
+  merge_kernel<<<grid_for(rows, 256 / lpr), 256, 0, s>>>(n_parts, o_parts, lse_parts, B, L, H, D,
+                                                         lpr, out, out_fp32, lse);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_pre(const void* out, int out_fp32, const void* dout, const float* lse,
-                           float* Dsm, float* L2sm, int B, int64_t L, int H, int D, int P,
-                           int layout, cudaStream_t s) {
+                           float* Dsm, float* L2sm, float* dq_acc, int B, int64_t L, int H, int D,
+                           int P, int layout, cudaStream_t s) {
+  if (D % 8 != 0 || D < 8 || D > 256 || (D & (D - 1)) != 0) return cudaErrorInvalidValue;
   const long long rows = (long long)B * L * H;
-  bwd_pre_kernel<<<grid_for(rows, 8), 256, 0, s>>>(
-      out, out_fp32, reinterpret_cast<const __nv_bfloat16*>(dout), lse, Dsm, L2sm, B, L, H, D, P,
-      layout);
+  bwd_pre_kernel<<<grid_for(rows, 256 / (D / 8)), 256, 0, s>>>(
+      out, out_fp32, reinterpret_cast<const __nv_bfloat16*>(dout), lse, Dsm, L2sm, dq_acc, B, L,
+      H, D, P, layout);
   return cudaGetLastError();
 }
 

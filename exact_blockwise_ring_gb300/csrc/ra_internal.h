@@ -172,8 +172,8 @@ cudaError_t launch_merge(int n_parts, const float* o_parts, const float* lse_par
                          int64_t L, int H, int D, void* out, int out_fp32, float* lse,
                          cudaStream_t s);
 cudaError_t launch_bwd_pre(const void* out, int out_fp32, const void* dout, const float* lse,
-                           float* Dsm, float* L2sm, int B, int64_t L, int H, int D, int P,
-                           int layout, cudaStream_t s);
+                           float* Dsm, float* L2sm, float* dq_acc, int B, int64_t L, int H, int D,
+                           int P, int layout, cudaStream_t s);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, float scale, size_t n,
                               cudaStream_t s);
 cudaError_t launch_selftest_timeout(unsigned int* err, uint64_t limit_ns, cudaStream_t s);

@@ -146,14 +146,17 @@ def test_layouts_agree_and_runs_are_deterministic():
     assert float((lz - ls).abs().max()) <= LSE_TOL
 
 
-def test_merge_entry_point_matches_oracle_merge():
-    rng = np.random.default_rng(3)
-    n, B, L, H, D = 3, 1, 256, 2, 128
+@pytest.mark.parametrize("n,D", [(3, 128), (6, 128), (1, 64), (5, 24), (2, 256)])
+def test_merge_entry_point_matches_oracle_merge(n, D):
+    rng = np.random.default_rng(3 + n + D)
+    B, L, H = 1, 256, 2
     o = rng.standard_normal((n, B, L, H, D)).astype(np.float32)
     lse = rng.standard_normal((n, B, H, L)).astype(np.float32)
-    lse[1, 0, 0, :7] = -np.inf
+    lse[n - 1, 0, 0, :7] = -np.inf
+    o[n - 1, 0, :7, 0, :] = np.nan                  # a skipped partial's contents never matter
     lse[:, 0, 1, 5] = -np.inf                       # a row with no visible key at all
-    mo, ml = oracle.merge_partials(o.astype(np.float64), lse.astype(np.float64))
+    o_or = np.where(np.isnan(o), 0.0, o).astype(np.float64)
+    mo, ml = oracle.merge_partials(o_or, lse.astype(np.float64))
     go, gl = era.ra_merge(torch.from_numpy(o).cuda(), torch.from_numpy(lse).cuda(),
                           out_dtype=torch.float32)
     torch.cuda.synchronize()
