@@ -15,6 +15,8 @@ Sources (four web pages on Ring Attention and Striped Attention):
 * "Ring Attention: Sequence Parallelism for Long Context" (vanos001): the ring
   diagram, the striped assignment (section "The Causal-Mask Problem: Striped
   Attention") and the worked demo of per-device work (section "Worked Demo").
+* the same labhub page, section "BPT の Feedforward 融合": the blockwise transformer
+  layer (attention fused with the feed-forward network per query block).
 * "Sequence parallelism and ring attention" (aiunderstanding) and the Striped
   Attention summary (aibr.jp, section 3, permutation equivariance).
 
@@ -27,6 +29,8 @@ Modules:
     work      -- shard assignment, ring order and the per-shard work model.
     gqa       -- grouped-query attention (fewer key/value heads than query heads) on top
                  of ``attention``.
+    bpt       -- one Blockwise Parallel Transformer layer (projections, attention, output
+                 projection, residuals, LayerNorms, GELU feed-forward), forward.
 
 Parity status: every function here is pinned by tests in ``tests/test_oracle_*.py``
 against things other than itself (a library softmax attention, closed forms,
@@ -39,10 +43,11 @@ from .ring import ring_fwd, ring_partials, merge_partials
 from .work import (shard_of, local_of, shard_tokens, ring_order, shard_work,
                    tile_class)
 from .gqa import gqa_fwd, gqa_bwd, group_size
+from .bpt import bpt_layer_fwd, bpt_layer_fwd_blocked, gelu, layer_norm
 
 __all__ = [
     "attention_fwd", "attention_bwd", "attention_rows_fwd", "attention_rows_dq", "brute_force_fwd",
     "default_scale", "ring_fwd", "ring_partials", "merge_partials", "shard_of",
     "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class", "gqa_fwd", "gqa_bwd",
-    "group_size",
+    "group_size", "bpt_layer_fwd", "bpt_layer_fwd_blocked", "gelu", "layer_norm",
 ]

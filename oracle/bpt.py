@@ -1,0 +1,107 @@
+"""One Blockwise Parallel Transformer layer, forward, in fp64.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Source: labhub "Ring Attention 論文分析", section "BPT の Feedforward 融合": the layer
+projects the input to Q, K, V, and then, one query block at a time, takes that block's
+attention over all keys, applies the output projection, adds the block's input and
+normalises, applies the feed-forward network (Linear, GELU, Linear), adds the normalised
+value and normalises again, and writes the block's output.  Only the current block's
+intermediates are ever held, which is the point of the fusion; the result is the plain
+post-norm transformer layer.  Written out, for x [B, L, d]:
+
+    Q = x Wq^T + bq,  K = x Wk^T + bk,  V = x Wv^T + bv          (Linear: y = x W^T + b)
+    A = attention(Q, K, V) over n_heads heads of d_k = d / n_heads (head h = features
+        [h d_k, (h+1) d_k)), causal or not, scale 1 / sqrt(d_k)
+    h1 = LN1(x + A Wo^T + bo)
+    out = LN2(h1 + (GELU(h1 W1^T + b1)) W2^T + b2)
+
+    LN(y) = (y - mean(y)) / sqrt(var(y) + eps) * gamma + beta over the d features of a row,
+            var the biased (population) variance, eps = 1e-5;
+    GELU(z) = z * Phi(z) = z / 2 * (1 + erf(z / sqrt(2)))   (the exact form).
+
+The page's layer shows no mask; the attention here takes the same `causal` switch as the
+rest of this package.  Weights follow torch.nn.Linear's layout: W [out_features,
+in_features].  ``bpt_layer_fwd`` computes the whole sequence at once;
+``bpt_layer_fwd_blocked`` follows the page's loop over query blocks and is used by the
+tests to show that the two agree (the fusion changes memory, not the result).
+"""
+
+import math
+
+import numpy as np
+
+from .attention import attention_fwd
+
+LN_EPS = 1e-5
+
+WEIGHT_NAMES = ("wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo", "w1", "b1", "w2", "b2",
+                "ln1_g", "ln1_b", "ln2_g", "ln2_b")
+
+
+def _erf(z):
+    return np.vectorize(math.erf, otypes=[np.float64])(z)
+
+
+def gelu(z):
+    """Exact GELU, z * Phi(z)."""
+    return 0.5 * z * (1.0 + _erf(z / math.sqrt(2.0)))
+
+
+def layer_norm(y, g, b, eps=LN_EPS):
+    mu = y.mean(axis=-1, keepdims=True)
+    var = ((y - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (y - mu) / np.sqrt(var + eps) * g + b
+
+
+def linear(x, w, b):
+    return x @ w.T + b
+
+
+def _heads(t, n_heads):
+    B, L, d = t.shape
+    return t.reshape(B, L, n_heads, d // n_heads)
+
+
+def _post_attention(xb, ab, w):
+    """Output projection, residual, LN1, FFN, residual, LN2 for rows xb with attention ab."""
+    h1 = layer_norm(xb + linear(ab, w["wo"], w["bo"]), w["ln1_g"], w["ln1_b"])
+    f = linear(gelu(linear(h1, w["w1"], w["b1"])), w["w2"], w["b2"])
+    return layer_norm(h1 + f, w["ln2_g"], w["ln2_b"])
+
+
+def bpt_layer_fwd(x, w, n_heads, causal):
+    """x [B, L, d] float64, w dict of float64 arrays (WEIGHT_NAMES).  Returns [B, L, d]."""
+    B, L, d = x.shape
+    q = _heads(linear(x, w["wq"], w["bq"]), n_heads)
+    k = _heads(linear(x, w["wk"], w["bk"]), n_heads)
+    v = _heads(linear(x, w["wv"], w["bv"]), n_heads)
+    a, _ = attention_fwd(q, k, v, causal)
+    return _post_attention(x, a.reshape(B, L, d), w)
+
+
+def bpt_layer_fwd_blocked(x, w, n_heads, causal, block_size):
+    """The page's loop: per query block, attention over all keys, then the rest."""
+    B, L, d = x.shape
+    if L % block_size:
+        raise ValueError("seq_len must be a multiple of block_size")
+    q = linear(x, w["wq"], w["bq"])
+    k = _heads(linear(x, w["wk"], w["bk"]), n_heads)
+    v = _heads(linear(x, w["wv"], w["bv"]), n_heads)
+    out = np.zeros_like(x)
+    dk = d // n_heads
+    for s in range(0, L, block_size):
+        qb = _heads(q[:, s:s + block_size], n_heads)
+        # attention of this block's queries over all keys: masked by original positions
+        # (query s + r sees keys <= s + r when causal)
+        sc = np.einsum("brhd,bchd->bhrc", qb, k) / math.sqrt(dk)
+        if causal:
+            r = np.arange(block_size)[:, None] + s
+            c = np.arange(L)[None, :]
+            sc = np.where(c <= r, sc, -np.inf)
+        sc = sc - sc.max(axis=-1, keepdims=True)
+        p = np.exp(sc)
+        p /= p.sum(axis=-1, keepdims=True)
+        ab = np.einsum("bhrc,bchd->brhd", p, v).reshape(B, block_size, d)
+        out[:, s:s + block_size] = _post_attention(x[:, s:s + block_size], ab, w)
+    return out

@@ -1,0 +1,126 @@
+"""Pins for the oracle's Blockwise Parallel Transformer layer (CPU only).
+
+References: torch's library modules in float64 (nn.Linear, nn.LayerNorm, nn.GELU with
+its exact erf form, scaled_dot_product_attention), the page's own per-block loop (the
+fusion must not change the result), the normal CDF for GELU, and the moments of a
+LayerNorm output.  Planted mistakes (tanh GELU, unbiased variance, no first residual)
+are shown to fail the library pin.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import bpt as obpt
+
+
+def _weights(d, d_ff, seed):
+    rng = np.random.default_rng(seed)
+    w = {}
+    for name, (o, i) in (("wq", (d, d)), ("wk", (d, d)), ("wv", (d, d)), ("wo", (d, d)),
+                         ("w1", (d_ff, d)), ("w2", (d, d_ff))):
+        w[name] = rng.standard_normal((o, i)) / math.sqrt(i)
+        w["b" + name[1:]] = 0.1 * rng.standard_normal(o)
+    for ln in ("ln1", "ln2"):
+        w[ln + "_g"] = 1.0 + 0.1 * rng.standard_normal(d)
+        w[ln + "_b"] = 0.1 * rng.standard_normal(d)
+    return w
+
+
+def _torch_layer(x, w, n_heads, causal):
+    """The same layer from torch's library modules, float64."""
+    d = x.shape[-1]
+    d_ff = w["w1"].shape[0]
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a))   # noqa: E731
+    lin = {}
+    for name, (o, i) in (("q", (d, d)), ("k", (d, d)), ("v", (d, d)), ("o", (d, d)),
+                         ("1", (d_ff, d)), ("2", (d, d_ff))):
+        m = torch.nn.Linear(i, o, dtype=torch.float64)
+        with torch.no_grad():
+            m.weight.copy_(T(w["w" + name]))
+            m.bias.copy_(T(w["b" + name]))
+        lin[name] = m
+    lns = []
+    for ln in ("ln1", "ln2"):
+        m = torch.nn.LayerNorm(d, eps=1e-5, dtype=torch.float64)
+        with torch.no_grad():
+            m.weight.copy_(T(w[ln + "_g"]))
+            m.bias.copy_(T(w[ln + "_b"]))
+        lns.append(m)
+    xt = T(x)
+    B, L, _ = x.shape
+    split = lambda t: t.view(B, L, n_heads, d // n_heads).transpose(1, 2)   # noqa: E731
+    with torch.no_grad():
+        a = F.scaled_dot_product_attention(split(lin["q"](xt)), split(lin["k"](xt)),
+                                           split(lin["v"](xt)), is_causal=causal)
+        a = a.transpose(1, 2).reshape(B, L, d)
+        h1 = lns[0](xt + lin["o"](a))
+        f = lin["2"](torch.nn.GELU()(lin["1"](h1)))
+        return lns[1](h1 + f).numpy()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,L,d,H,d_ff", [(1, 64, 32, 2, 64), (2, 96, 48, 3, 96),
+                                          (1, 128, 64, 1, 256)])
+def test_layer_matches_library_modules(causal, B, L, d, H, d_ff):
+    w = _weights(d, d_ff, seed=L + d)
+    x = np.random.default_rng(L).standard_normal((B, L, d))
+    got = oracle.bpt_layer_fwd(x, w, H, causal)
+    want = _torch_layer(x, w, H, causal)
+    assert np.max(np.abs(got - want)) < 1e-10
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("block", [16, 32, 128])
+def test_blockwise_loop_equals_whole_sequence(causal, block):
+    w = _weights(32, 64, seed=3)
+    x = np.random.default_rng(4).standard_normal((2, 128, 32))
+    a = oracle.bpt_layer_fwd(x, w, 2, causal)
+    b = oracle.bpt_layer_fwd_blocked(x, w, 2, causal, block)
+    assert np.max(np.abs(a - b)) < 1e-11
+
+
+def test_gelu_is_z_times_normal_cdf():
+    z = np.array([-3.0, -1.0, 0.0, 0.5, 1.0, 2.0, 6.0])
+    # Phi(1) and Phi(-1) to 16 digits, Phi(0) = 1/2
+    assert abs(oracle.gelu(np.array([1.0]))[0] - 0.8413447460685429) < 1e-15
+    assert abs(oracle.gelu(np.array([-1.0]))[0] + 0.15865525393145707) < 1e-15
+    assert oracle.gelu(np.array([0.0]))[0] == 0.0
+    from scipy.stats import norm
+    assert np.max(np.abs(oracle.gelu(z) - z * norm.cdf(z))) < 1e-15
+
+
+def test_layer_norm_moments():
+    y = np.random.default_rng(5).standard_normal((7, 64)) * 3.0 + 2.0
+    out = oracle.layer_norm(y, np.ones(64), np.zeros(64))
+    var = y.var(axis=-1)
+    assert np.max(np.abs(out.mean(axis=-1))) < 1e-14
+    assert np.max(np.abs(out.var(axis=-1) - var / (var + 1e-5))) < 1e-12
+
+
+def test_planted_mistakes_fail_the_library_pin(monkeypatch):
+    w = _weights(32, 64, seed=6)
+    x = np.random.default_rng(7).standard_normal((1, 64, 32))
+    want = _torch_layer(x, w, 2, True)
+
+    def tanh_gelu(z):
+        return 0.5 * z * (1 + np.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3)))
+
+    def unbiased_ln(y, g, b, eps=1e-5):
+        return (y - y.mean(-1, keepdims=True)) / np.sqrt(y.var(-1, ddof=1, keepdims=True) + eps) * g + b
+
+    def no_residual(xb, ab, ww):
+        h1 = obpt.layer_norm(obpt.linear(ab, ww["wo"], ww["bo"]), ww["ln1_g"], ww["ln1_b"])
+        f = obpt.linear(obpt.gelu(obpt.linear(h1, ww["w1"], ww["b1"])), ww["w2"], ww["b2"])
+        return obpt.layer_norm(h1 + f, ww["ln2_g"], ww["ln2_b"])
+
+    for attr, fake in (("gelu", tanh_gelu), ("layer_norm", unbiased_ln),
+                       ("_post_attention", no_residual)):
+        with monkeypatch.context() as mp:
+            mp.setattr(obpt, attr, fake)
+            got = obpt.bpt_layer_fwd(x, w, 2, True)
+        assert np.max(np.abs(got - want)) > 1e-6, attr
