@@ -6,7 +6,8 @@ then the backward's three stages (preprocess, main kernel, dQ finalize).  FLOPs 
 causal-useful work only: per unmasked (query, key) pair 4*D forward and 10*D backward
 (five products, the recompute included).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 32k|262k|1m|8k|32k-gqa]
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+                  [--workload 32k|262k|1m|8k|32k-gqa|32k-bpt]
                   [--layout striped|contiguous|zigzag] [--impl ours|reference]
 
 N > 1 runs under torchrun: every rank runs an independent replica on its own GPU (the
@@ -38,7 +39,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="32k", choices=["8k", "32k", "262k", "1m", "32k-gqa"])
+    ap.add_argument("--workload", default="32k",
+                    choices=["8k", "32k", "262k", "1m", "32k-gqa", "32k-bpt"])
     ap.add_argument("--layout", default=None, choices=["striped", "contiguous", "zigzag"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -80,7 +82,8 @@ def peaks():
 def config_of(w):
     L, H, D = w["seq_len"], w["heads"], w["head_dim"]
     tensor_mib = w["batch"] * L * H * D * 2 / 2 ** 20
-    return {"workload": "%s causal fwd+bwd, %s layout" % (w["name"], w["layout"]),
+    what = "one blockwise transformer layer forward" if "d_ff" in w else "causal fwd+bwd"
+    return {"workload": "%s %s, %s layout" % (w["name"], what, w["layout"]),
             "batch": w["batch"], "heads": H, "kv_heads": w.get("kv_heads", H),
             "head_dim": D, "seq_len": L, "P": w["P"],
             "block": w["block"], "layout": w["layout"], "causal": w["causal"],
@@ -401,20 +404,172 @@ def run_ours(args, w, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- BPT layer --------
+BPT_METRIC = "blockwise transformer layer forward TFLOP/s (projections, causal ring attention, FFN)"
+
+
+def bpt_flops(w):
+    """Useful FLOPs of one layer forward: Q, K, V, O projections 4 * 2 L d^2, feed-forward
+    2 * 2 L d d_ff, causal attention 4 D per unmasked pair per head."""
+    rows = w["batch"] * w["seq_len"]
+    d = w["heads"] * w["head_dim"]
+    attn = 4 * w["head_dim"] * w["batch"] * w["heads"] * pairs_of(w["seq_len"], w["causal"])
+    return 8 * rows * d * d + 4 * rows * d * w["d_ff"] + attn
+
+
+def bpt_oracle_sample(w, tokens=1024, d=1024, d_ff=4096):
+    """fp64 oracle layer forward on a bounded sample: 1 x `tokens` x d, d_ff, 4 heads."""
+    import numpy as np
+    import oracle
+    from exact_blockwise_ring_gb300.synthetic import make_bpt_weights, to_f64
+    rng = np.random.default_rng(w["seed"])
+    x = rng.standard_normal((1, tokens, d))
+    wt = {k: to_f64(v)[0] for k, v in make_bpt_weights(d, d_ff, w["seed"]).items()}
+    t0 = time.perf_counter()
+    oracle.bpt_layer_fwd(x, wt, d // 128, w["causal"])
+    t = time.perf_counter() - t0
+    sw = dict(w, batch=1, seq_len=tokens, heads=d // 128, head_dim=128, d_ff=d_ff)
+    return t, bpt_flops(sw) / 1e12, len(os.sched_getaffinity(0))
+
+
+def run_bpt(args, w, rank, world, local):
+    import torch
+    import exact_blockwise_ring_gb300 as era
+    from exact_blockwise_ring_gb300.synthetic import make_bpt_weights, make_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, L, H, D, P, blk = (w["batch"], w["seq_len"], w["heads"], w["head_dim"], w["P"],
+                          w["block"])
+    d, d_ff, br = H * D, w["d_ff"], w["block_rows"]
+    x = make_inputs(B, L, 1, d, w["seed"] + 7919 * rank, device=dev, with_dout=False)[0]
+    x = x.view(B, L, d)
+    wt = make_bpt_weights(d, d_ff, w["seed"] + 1, device=dev)
+    out = torch.empty((B, L, d), dtype=torch.bfloat16, device=dev)
+    ws = era.Workspace(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        era.ra_bpt_fwd(x, wt, H, P, blk, w["layout"], w["causal"], block_rows=br, workspace=ws,
+                       out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ws.check()
+    dist_barrier(world)
+    K = args.steps
+    clocks = ClockSampler(None)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clk = clocks.stop()
+    ws.check()
+    total_ms = dist_max(t0.elapsed_time(t1), world)
+    flops = bpt_flops(w)
+    value = world * flops * K / (total_ms * 1e-3) / 1e12
+
+    # dominant kernel: the feed-forward GEMM of one block (rows br, d -> d_ff, GELU), timed
+    # alone with CUDA events on the launching stream
+    pk, pk_kind = peaks()
+    peak_tf = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    h1 = torch.randn((br, d), device=dev).to(torch.bfloat16)
+    f = torch.empty((br, d_ff), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        era.ra_linear(h1, wt["w1"], wt["b1"], "bias_gelu", workspace=ws, out=f)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    reps = 10
+    g0.record(stream)
+    for _ in range(reps):
+        era.ra_linear(h1, wt["w1"], wt["b1"], "bias_gelu", workspace=ws, out=f)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    ws.check()
+    g_ms = g0.elapsed_time(g1) / reps
+    g_tf = 2.0 * br * d * d_ff / (g_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel (FFN W1 + bias + GELU)",
+                "achieved": round(g_tf, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(g_tf / peak_tf, 4), "peak_kind": "bf16_tflops (burst) of %s" % pk_kind,
+                "traffic": None, "shape": [br, d_ff, d]}
+
+    e2e = None
+    if not args.no_e2e:
+        hx = x.cpu().pin_memory()
+        ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = dist_max(a0.elapsed_time(a1), world)
+        e2e = {"value": round(world * flops * K / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": ho.numel() * 2,
+               "ms_per_step": round(e_ms / K, 3)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        t, tf, cores = bpt_oracle_sample(w)
+        cpu = {"value": tf / t, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": "fp64 oracle layer forward, 1 x 1024 tokens, d 1024, d_ff 4096, 8 heads, "
+                         "causal, %.1f s; useful-FLOP convention of the GPU line" % t}
+    n_blocks = -(-(B * L) // br)
+    # per step: 3 projection GEMMs, the attention (1 kernel, + merge when split), and per
+    # block 3 GEMMs and 2 LayerNorms
+    launches = 3 + 1 + 5 * n_blocks
+    if rank == 0:
+        line = {"metric": BPT_METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+                "n_gpus": world, "steps": K, "warmup": args.warmup,
+                "ms_per_step": round(total_ms / K, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
+                "config": {"workload": "%s: one blockwise transformer layer forward, %s layout"
+                           % (w["name"], w["layout"]), "batch": B, "seq_len": L, "d_model": d,
+                           "heads": H, "d_ff": d_ff, "P": P, "block": blk, "block_rows": br,
+                           "causal": w["causal"], "flops_per_step": flops,
+                           "l2": "inputs larger than L2 (x %.0f MiB, weights %.0f MiB)"
+                           % (x.numel() * 2 / 2 ** 20,
+                              sum(t.numel() * t.element_size() for t in wt.values()) / 2 ** 20)},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches * K, "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- reference arm ----
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
+    bpt = "d_ff" in w
     t_steps = []
     for s in range(args.warmup + args.steps):
-        t, tf, cores = oracle_sample(w, REF_STEP_TOKENS)
+        t, tf, cores = bpt_oracle_sample(w) if bpt else oracle_sample(w, REF_STEP_TOKENS)
         if s >= args.warmup:
             t_steps.append(t)
     total = sum(t_steps)
     value = tf * len(t_steps) / total
-    sample = ("fp64 oracle fwd+bwd per step: 1 head x %d tokens (causal) of the workload's "
-              "input distribution; useful-FLOP convention of the GPU line" % REF_STEP_TOKENS)
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5),
+    if bpt:
+        sample = ("fp64 oracle layer forward per step: 1 x 1024 tokens, d 1024, d_ff 4096, "
+                  "8 heads, causal; useful-FLOP convention of the GPU line")
+    else:
+        sample = ("fp64 oracle fwd+bwd per step: 1 head x %d tokens (causal) of the workload's "
+                  "input distribution; useful-FLOP convention of the GPU line" % REF_STEP_TOKENS)
+    line = {"impl": "reference", "metric": BPT_METRIC if bpt else METRIC, "value": round(value, 5),
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * total / len(t_steps), 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -426,7 +581,6 @@ def run_reference(args, w, rank, world):
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
 
-
 def main():
     args = parse_args()
     w = workload(args.workload, args.layout)
@@ -437,7 +591,10 @@ def main():
         return
     rank, world, local = dist_init(args)
     try:
-        run_ours(args, w, rank, world, local)
+        if "d_ff" in w:
+            run_bpt(args, w, rank, world, local)
+        else:
+            run_ours(args, w, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist

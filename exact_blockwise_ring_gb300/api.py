@@ -31,6 +31,24 @@ class Params(ctypes.Structure):
                 ("kv_heads", ctypes.c_int)]
 
 
+class BptParams(ctypes.Structure):
+    """Mirror of ra_bpt_params_t."""
+    _fields_ = [("attn", Params), ("d_ff", ctypes.c_int), ("block_rows", ctypes.c_int64),
+                ("ln_eps", ctypes.c_float)]
+
+
+BPT_WEIGHTS = ("wq", "wk", "wv", "wo", "w1", "w2", "bq", "bk", "bv", "bo", "b1", "b2",
+               "ln1_g", "ln1_b", "ln2_g", "ln2_b")
+
+
+class BptWeights(ctypes.Structure):
+    """Mirror of ra_bpt_weights_t (device pointers)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in BPT_WEIGHTS]
+
+
+EPILOGUES = {"bias": 0, "bias_gelu": 1, "bias_residual": 2}
+
+
 class RaError(RuntimeError):
     def __init__(self, status, message):
         self.status = status
@@ -60,6 +78,13 @@ _SIGS = {
     "ra_check_error": (ctypes.c_int, [_P, _P]),
     "ra_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint, _P]),
     "ra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ra_linear": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P,
+                                 ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
+    "ra_layernorm": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, _P, _P, _P, ctypes.c_float, _P,
+                                    ctypes.c_int, _P]),
+    "ra_bpt_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(BptParams)]),
+    "ra_bpt_fwd": (ctypes.c_int, [ctypes.POINTER(BptParams), _P, ctypes.POINTER(BptWeights), _P,
+                                  ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "ra_last_error_message": (ctypes.c_char_p, []),
 }
 
@@ -256,6 +281,63 @@ def ra_shard_work_model(seq_len, P, block, layout, causal):
 def ra_selftest_timeout(workspace, timeout_us, stream=None):
     buf = workspace.get(256)
     _check(lib().ra_selftest_timeout(_ptr(buf), buf.numel(), int(timeout_us), _stream(stream)))
+
+
+def ra_linear(x, weight, bias, epilogue="bias", residual=None, workspace=None, stream=None,
+              out=None):
+    """out = epilogue(x weight^T + bias) through ra_linear.  x [..., in] bf16, weight
+    [out, in] bf16, bias [out] fp32; "bias" / "bias_gelu" give bf16, "bias_residual" adds
+    residual [..., out] bf16 and gives fp32."""
+    epi = EPILOGUES[epilogue]
+    rows = x.numel() // x.shape[-1]
+    n_out, n_in = weight.shape
+    shape = tuple(x.shape[:-1]) + (n_out,)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32 if epi == 2 else torch.bfloat16,
+                          device=x.device)
+    ws = workspace or default_workspace(x.device)
+    buf = ws.get(256)
+    _check(lib().ra_linear(rows, n_in, n_out, _ptr(x), _ptr(weight), _ptr(bias), _ptr(residual),
+                           epi, _ptr(out), _ptr(buf), buf.numel(), _stream(stream)))
+    return out
+
+
+def ra_layernorm(x, gamma, beta, eps=1e-5, out_dtype=torch.bfloat16, stream=None):
+    """LayerNorm over the last dimension of fp32 x through ra_layernorm."""
+    d = x.shape[-1]
+    out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    odt = RA_FP32 if out_dtype == torch.float32 else RA_BF16
+    _check(lib().ra_layernorm(x.numel() // d, d, _ptr(x), _ptr(gamma), _ptr(beta), float(eps),
+                              _ptr(out), odt, _stream(stream)))
+    return out
+
+
+def make_bpt_params(batch, seq_len, heads, head_dim, d_ff, P, block, layout="contiguous",
+                    causal=True, block_rows=0, ln_eps=0.0, n_split=0):
+    return BptParams(make_params(batch, seq_len, heads, head_dim, P, block, layout, causal, 0.0,
+                                 n_split, 0), int(d_ff), int(block_rows), float(ln_eps))
+
+
+def bpt_workspace_bytes(params):
+    return lib().ra_bpt_workspace_bytes(ctypes.byref(params))
+
+
+def ra_bpt_fwd(x, weights, heads, P, block, layout="contiguous", causal=True, block_rows=0,
+               out_dtype=torch.bfloat16, workspace=None, stream=None, out=None):
+    """One blockwise transformer layer forward through ra_bpt_fwd.  x [B, L, d] bf16;
+    weights: dict with the names of BPT_WEIGHTS (weights bf16 [out, in], the rest fp32)."""
+    B, L, d = x.shape
+    d_ff = weights["w1"].shape[0]
+    prm = make_bpt_params(B, L, heads, d // heads, d_ff, P, block, layout, causal, block_rows)
+    w = BptWeights(*[weights[n].data_ptr() for n in BPT_WEIGHTS])
+    if out is None:
+        out = torch.empty((B, L, d), dtype=out_dtype, device=x.device)
+    odt = RA_FP32 if out.dtype == torch.float32 else RA_BF16
+    ws = workspace or default_workspace(x.device)
+    buf = ws.get(max(bpt_workspace_bytes(prm), 256))
+    _check(lib().ra_bpt_fwd(ctypes.byref(prm), _ptr(x), ctypes.byref(w), _ptr(out), odt,
+                            _ptr(buf), buf.numel(), _stream(stream)))
+    return out
 
 
 class RingAttention(torch.autograd.Function):

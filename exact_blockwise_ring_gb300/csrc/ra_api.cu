@@ -218,6 +218,21 @@ void work_model(const ra_params_t* p, unsigned long long* outp) {
 
 void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
 
+ra_status_t encode_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                           uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return RA_OK;
+}
+
 }  // namespace ra
 
 using namespace ra;

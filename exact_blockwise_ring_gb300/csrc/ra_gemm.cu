@@ -1,0 +1,307 @@
+// ra_gemm.cu -- the dense kernels of the blockwise transformer layer (labhub "Ring Attention
+// 論文分析", section "BPT の Feedforward 融合"): a tcgen05 GEMM for its Linear layers with
+// the elementwise work fused into the epilogue, and a row LayerNorm.
+//
+// GEMM: out[M, N] = epilogue(A[M, K] B[N, K]^T + bias[N]), A and B bf16 row-major (B is a
+// torch.nn.Linear weight [out_features, in_features]), fp32 accumulation in TMEM.
+//   kEpiBias          out bf16 = acc + bias
+//   kEpiBiasGelu      out bf16 = GELU(acc + bias), GELU(z) = z/2 (1 + erf(z / sqrt 2))
+//   kEpiBiasResidual  out fp32 = acc + bias + residual[M, N] (bf16)
+// One CTA computes one 128 x 256 output tile.  Roles (192 threads):
+//   warp 0      TMA producer: per 64-wide K step one A box (128 x 64) and one B box
+//               (256 x 64), 128-byte swizzled, into a kStages-deep ring
+//   warp 1      TMEM owner (256 columns) and tcgen05.mma issuer: M = 128, N = 256, K = 16
+//               per instruction, both operands K-major from shared memory
+//   warps 2-5   epilogue, thread = output row = TMEM lane: 32 columns at a time out of
+//               TMEM, bias / GELU / residual in registers, 16-byte stores
+// CTAs walk the M tiles of one N tile before the next, so the resident CTAs share that
+// N tile of B in L2 and A (the activations) is re-read from L2 across N tiles.
+//
+// LayerNorm: y = (x - mean) / sqrt(var + eps) * gamma + beta per row, var the biased
+// variance, two passes over the row held in registers; 128 threads per row.
+#include <cuda_bf16.h>
+
+#include "ra_internal.h"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr int GM = 128, GN = 256, GK = 64, kStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kAB = GM * GK * 2;            // A box bytes (16 KB)
+constexpr int kBB = GN * GK * 2;            // B box bytes (32 KB)
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kAB;
+constexpr int kOffBar = kOffB + kStages * kBB;
+constexpr int kNBar = 2 * kStages + 1;      // full[], empty[], acc_full
+constexpr int kOffMisc = kOffBar + kNBar * 8;
+constexpr int kGemmSmem = kOffMisc + 16 + 1024;   // + alignment slack
+static_assert(kGemmSmem <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__device__ __forceinline__ float gelu_exact(float z) {
+  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = sm + kOffA;
+  uint8_t* sB = sm + kOffB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+  uint32_t* tmem_slot = misc;
+  volatile uint32_t* abort_flag = misc + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int mt = g.M / GM;
+  const int tm = blockIdx.x % mt, tn = blockIdx.x / mt;
+  const int m0 = tm * GM, n0 = tn * GN;
+  const int nk = g.K / GK;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = (*(volatile unsigned int*)g.err != 0u) ? 1u : 0u;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (*abort_flag) return;   // an earlier kernel gave up: uniform early exit
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = *tmem_slot;
+  const WaitCtx wc{abort_flag, g.err, g.wait_limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int kb = 0;
+      for (; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, wc)) break;
+        mbar_expect_tx(&full[s], kAB + kBB);
+        tma_load_2d(sA + s * kAB, &tmA, &full[s], kb * GK, m0);
+        tma_load_2d(sB + s * kBB, &tmB, &full[s], kb * GK, n0);
+      }
+      // let every copy this thread issued land before the CTA can exit
+      for (int r = (kb > kStages ? kb - kStages : 0); r < kb; ++r)
+        wait_drain(&full[r % kStages], (r / kStages) & 1, g.wait_limit_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(GM, GN, false, false);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (!mbar_wait(&full[s], (kb / kStages) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t ad = sdesc_kmajor(a0 + s * kAB), bd = sdesc_kmajor(b0 + s * kBB);
+#pragma unroll
+        for (int kk = 0; kk < GK / 16; ++kk)          // +32 bytes per K step of 16
+          umma_ss(tacc, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(acc_full);
+      if (!ok) wait_drain(acc_full, 0, g.wait_limit_ns);
+    }
+  } else {
+    // ================================================================ epilogue =====
+    const int q = warp & 3;                       // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;
+    const size_t row = (size_t)(m0 + r);
+    const uint32_t trow = tacc + (static_cast<uint32_t>(q * 32) << 16);
+    if (mbar_wait(acc_full, 0, wc)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < GN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(trow + 32 * c, v);
+        tmem_wait_ld();
+        const int col = n0 + 32 * c;
+        float f[32];
+        const float4* bias4 = reinterpret_cast<const float4*>(g.bias + col);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 bb = __ldg(bias4 + e);
+          f[4 * e + 0] = __uint_as_float(v[4 * e + 0]) + bb.x;
+          f[4 * e + 1] = __uint_as_float(v[4 * e + 1]) + bb.y;
+          f[4 * e + 2] = __uint_as_float(v[4 * e + 2]) + bb.z;
+          f[4 * e + 3] = __uint_as_float(v[4 * e + 3]) + bb.w;
+        }
+        if (EPI == kEpiBiasResidual) {
+          const uint4* res = reinterpret_cast<const uint4*>(
+              reinterpret_cast<const __nv_bfloat16*>(g.residual) + row * g.N + col);
+          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + row * g.N + col);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint4 w = __ldg(res + e);
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[x]));
+              f[8 * e + 2 * x] += p.x;
+              f[8 * e + 2 * x + 1] += p.y;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+        } else {
+          if (EPI == kEpiBiasGelu) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) f[e] = gelu_exact(f[e]);
+          }
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(g.out) + row * g.N + col);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            o[e] = make_uint4(pack_bf16x2(f[8 * e], f[8 * e + 1]), pack_bf16x2(f[8 * e + 2], f[8 * e + 3]),
+                              pack_bf16x2(f[8 * e + 4], f[8 * e + 5]),
+                              pack_bf16x2(f[8 * e + 6], f[8 * e + 7]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tacc, 256);
+  }
+}
+
+// LayerNorm of one row per CTA (128 threads, d / 128 features each, d % 512 == 0 and
+// d <= 8192): mean, then the biased variance of the deviations, both reduced in fp32.
+template <int OUT_FP32>
+__global__ void __launch_bounds__(128)
+    layernorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                     const float* __restrict__ beta, float eps, int d, void* out) {
+  constexpr int kMaxV = 16;                     // float4 per thread: d <= 16 * 512
+  __shared__ float red[2][4];
+  const size_t row = blockIdx.x;
+  const int nv = d / 512;
+  const float4* xr = reinterpret_cast<const float4*>(x + row * d);
+  float4 v[kMaxV];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+    if (i < nv) {
+      v[i] = __ldg(xr + i * 128 + threadIdx.x);
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) red[0][w] = s;
+  __syncthreads();
+  const float mean = (red[0][0] + red[0][1] + red[0][2] + red[0][3]) / d;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+    if (i < nv) {
+      const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
+      q += (a * a + b * b) + (c * c + e * e);
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  if (lane == 0) red[1][w] = q;
+  __syncthreads();
+  const float rstd = rsqrtf((red[1][0] + red[1][1] + red[1][2] + red[1][3]) / d + eps);
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+    if (i < nv) {
+      const int f0 = (i * 128 + threadIdx.x) * 4;
+      const float4 gg = __ldg(reinterpret_cast<const float4*>(gamma + f0));
+      const float4 bb = __ldg(reinterpret_cast<const float4*>(beta + f0));
+      const float y0 = (v[i].x - mean) * rstd * gg.x + bb.x;
+      const float y1 = (v[i].y - mean) * rstd * gg.y + bb.y;
+      const float y2 = (v[i].z - mean) * rstd * gg.z + bb.z;
+      const float y3 = (v[i].w - mean) * rstd * gg.w + bb.w;
+      if (OUT_FP32) {
+        reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * d)[i * 128 + threadIdx.x] =
+            make_float4(y0, y1, y2, y3);
+      } else {
+        reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * d)[i * 128 + threadIdx.x] =
+            make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+      }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb, int epi,
+                        cudaStream_t s) {
+  const long long grid = (long long)(g.M / GM) * (g.N / GN);
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e;
+  switch (epi) {
+    case kEpiBias:
+      e = cudaFuncSetAttribute(gemm_kernel<kEpiBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kGemmSmem);
+      if (e != cudaSuccess) return e;
+      gemm_kernel<kEpiBias><<<(unsigned)grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, g);
+      break;
+    case kEpiBiasGelu:
+      e = cudaFuncSetAttribute(gemm_kernel<kEpiBiasGelu>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+      if (e != cudaSuccess) return e;
+      gemm_kernel<kEpiBiasGelu><<<(unsigned)grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, g);
+      break;
+    case kEpiBiasResidual:
+      e = cudaFuncSetAttribute(gemm_kernel<kEpiBiasResidual>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+      if (e != cudaSuccess) return e;
+      gemm_kernel<kEpiBiasResidual><<<(unsigned)grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, g);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm(const float* x, const float* gamma, const float* beta, float eps,
+                             long long rows, int d, void* out, int out_fp32, cudaStream_t s) {
+  if (d % 512 != 0 || d > 8192 || rows <= 0 || rows > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (out_fp32)
+    layernorm_kernel<1><<<(unsigned)rows, 128, 0, s>>>(x, gamma, beta, eps, d, out);
+  else
+    layernorm_kernel<0><<<(unsigned)rows, 128, 0, s>>>(x, gamma, beta, eps, d, out);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

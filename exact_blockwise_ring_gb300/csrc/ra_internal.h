@@ -163,6 +163,23 @@ struct BwdArgs {
   uint64_t wait_limit_ns;
 };
 
+// Dense kernels of the blockwise transformer layer (ra_gemm.cu).
+enum GemmEpilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResidual = 2 };
+
+struct GemmArgs {
+  int M, N, K;              // out[M, N] = A[M, K] B[N, K]^T; M % 128, N % 256, K % 64 == 0
+  const float* bias;        // [N] fp32
+  const void* residual;     // [M, N] bf16 (kEpiBiasResidual)
+  void* out;                // [M, N] bf16, or fp32 for kEpiBiasResidual
+  unsigned int* err;        // workspace error word
+  uint64_t wait_limit_ns;
+};
+
+cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb, int epi,
+                        cudaStream_t s);
+cudaError_t launch_layernorm(const float* x, const float* gamma, const float* beta, float eps,
+                             long long rows, int d, void* out, int out_fp32, cudaStream_t s);
+
 // Launchers (defined next to their kernels).
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s);
@@ -180,5 +197,10 @@ cudaError_t launch_selftest_timeout(unsigned int* err, uint64_t limit_ns, cudaSt
 
 // Sets the text ra_last_error_message() returns on this thread.
 void set_last_error_message(const char* msg);
+
+// A 2-D bf16 [outer, inner] row-major tensor map with 128-byte swizzled boxes of
+// box_outer rows x box_inner elements (ra_api.cu).
+ra_status_t encode_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                           uint32_t box_inner, uint32_t box_outer);
 
 }  // namespace ra

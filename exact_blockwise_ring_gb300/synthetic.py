@@ -23,9 +23,15 @@ WORKLOADS = {
     # grouped-query attention: 32 query heads on 8 key/value heads (4 per group)
     "32k-gqa": dict(batch=1, heads=32, kv_heads=8, head_dim=128, seq_len=32768, P=8,
                     block=128, causal=True, layouts=("zigzag", "striped"), backward=True),
+    # one blockwise transformer layer (forward): d_model 4096 = 32 x 128, d_ff = 4 d_model,
+    # the feed-forward part in blocks of 16384 rows
+    "32k-bpt": dict(batch=1, heads=32, head_dim=128, seq_len=32768, P=8, block=128,
+                    causal=True, layouts=("zigzag", "striped"), backward=False, d_ff=16384,
+                    block_rows=16384),
 }
 
-SEEDS = {"tiny": 1000, "8k": 1001, "32k": 1002, "262k": 1003, "1m": 1004, "32k-gqa": 1005}
+SEEDS = {"tiny": 1000, "8k": 1001, "32k": 1002, "262k": 1003, "1m": 1004, "32k-gqa": 1005,
+         "32k-bpt": 1006}
 
 
 def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=True,
@@ -49,6 +55,27 @@ def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=T
                         dtype=torch.float32)
         out.append(x.to(torch.bfloat16))
     return tuple(out)
+
+
+def make_bpt_weights(d, d_ff, seed, device="cpu"):
+    """Random parameters of one blockwise transformer layer: Linear weights [out, in] drawn
+    N(0, 1/in) and rounded to bf16, biases N(0, 0.01) fp32, LayerNorm scales 1 + N(0, 0.01)
+    and shifts N(0, 0.01) fp32 (N(mean, variance)), drawn in the order wq, wk, wv, wo, w1, w2,
+    bq, bk, bv, bo, b1, b2, ln1 scale, ln1 shift, ln2 scale, ln2 shift."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    shapes = {"wq": (d, d), "wk": (d, d), "wv": (d, d), "wo": (d, d), "w1": (d_ff, d),
+              "w2": (d, d_ff)}
+    w = {}
+    for name, (o, i) in shapes.items():
+        x = torch.randn((o, i), generator=g, device=device, dtype=torch.float32) / (i ** 0.5)
+        w[name] = x.to(torch.bfloat16)
+    for name, n in (("bq", d), ("bk", d), ("bv", d), ("bo", d), ("b1", d_ff), ("b2", d)):
+        w[name] = 0.1 * torch.randn(n, generator=g, device=device, dtype=torch.float32)
+    for ln in ("ln1", "ln2"):
+        w[ln + "_g"] = 1.0 + 0.1 * torch.randn(d, generator=g, device=device, dtype=torch.float32)
+        w[ln + "_b"] = 0.1 * torch.randn(d, generator=g, device=device, dtype=torch.float32)
+    return w
 
 
 def to_f64(*tensors):

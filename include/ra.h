@@ -228,6 +228,97 @@ ra_status_t ra_selftest_timeout(void* workspace, size_t workspace_bytes,
 const char* ra_status_string(ra_status_t s);
 const char* ra_last_error_message(void);
 
+/* ==================================================================================
+ * Blockwise Parallel Transformer layer, forward (labhub, section "BPT の Feedforward
+ * 融合"): Q, K, V projections, the ring attention above, then per block of rows the
+ * output projection, residual + LayerNorm, the feed-forward network (Linear, GELU,
+ * Linear), residual + LayerNorm:
+ *   h1  = LN1(x + attention(x Wq^T + bq, x Wk^T + bk, x Wv^T + bv) Wo^T + bo)
+ *   out = LN2(h1 + GELU(h1 W1^T + b1) W2^T + b2)
+ * Post-norm as on the page; LN uses the biased variance; GELU is the exact erf form.
+ * Only one block's feed-forward intermediates exist at a time, so the workspace grows
+ * with block_rows * d_ff, not with seq_len * d_ff.
+ * ================================================================================== */
+
+typedef enum {
+  RA_EPI_BIAS = 0,           /* out bf16 = x W^T + b                        */
+  RA_EPI_BIAS_GELU = 1,      /* out bf16 = GELU(x W^T + b)                  */
+  RA_EPI_BIAS_RESIDUAL = 2   /* out fp32 = x W^T + b + residual (bf16 [rows, out]) */
+} ra_epilogue_t;
+
+/*
+ * A Linear layer on tcgen05 tensor cores with its elementwise epilogue fused:
+ *   x [rows, in_features] bf16, weight [out_features, in_features] bf16 (torch.nn.Linear
+ *   layout), bias [out_features] fp32, residual (RA_EPI_BIAS_RESIDUAL only) [rows,
+ *   out_features] bf16, out [rows, out_features] bf16 or fp32 as listed above.
+ *   rows % 128 == 0, out_features % 256 == 0, in_features % 64 == 0 (else
+ *   RA_ERR_UNSUPPORTED); device pointers, 16-byte aligned.  workspace: >= 256 bytes,
+ *   zero-filled before first use; its first word is the error word (ra_check_error).
+ */
+ra_status_t ra_linear(int64_t rows, int in_features, int out_features, const void* x,
+                      const void* weight, const float* bias, const void* residual, int epilogue,
+                      void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * LayerNorm over the last dimension: out = (x - mean) / sqrt(var + eps) * gamma + beta,
+ * var the biased variance.  x fp32 [rows, features]; gamma, beta fp32 [features]; out
+ * [rows, features] of out_dtype.  features % 512 == 0 and <= 8192 (else
+ * RA_ERR_UNSUPPORTED); eps > 0.
+ */
+ra_status_t ra_layernorm(int64_t rows, int features, const float* x, const float* gamma,
+                         const float* beta, float eps, void* out, int out_dtype, void* stream);
+
+/*
+ * Layer description.
+ *   attn        the attention: batch, seq_len, heads, head_dim (d_model = heads *
+ *               head_dim), block, P, layout, causal, softmax_scale, n_split as for ra_fwd;
+ *               kv_heads must be 0 or heads (all three projections are d_model wide).
+ *   d_ff        feed-forward width, a multiple of 256.
+ *   block_rows  rows of the flattened [batch * seq_len] sequence per post-attention
+ *               block, a multiple of 128; 0 = min(batch * seq_len, 16384).
+ *   ln_eps      LayerNorm epsilon, 0 = 1e-5.
+ * d_model must be a multiple of 512 and at most 8192.
+ */
+typedef struct {
+  ra_params_t attn;
+  int d_ff;
+  int64_t block_rows;
+  float ln_eps;
+} ra_bpt_params_t;
+
+/* Layer parameters, all device pointers: weights bf16 in torch.nn.Linear layout
+ * [out, in] (wq, wk, wv, wo [d, d]; w1 [d_ff, d]; w2 [d, d_ff]), biases and LayerNorm
+ * scales / shifts fp32. */
+typedef struct {
+  const void* wq;
+  const void* wk;
+  const void* wv;
+  const void* wo;
+  const void* w1;
+  const void* w2;
+  const float* bq;
+  const float* bk;
+  const float* bv;
+  const float* bo;
+  const float* b1;
+  const float* b2;
+  const float* ln1_g;
+  const float* ln1_b;
+  const float* ln2_g;
+  const float* ln2_b;
+} ra_bpt_weights_t;
+
+/* Bytes of workspace ra_bpt_fwd needs (0 if `p` is invalid): the attention's workspace
+ * (whose error word is the layer's), Q, K, V and the attention output (bf16 [B*L, d]
+ * each), lse, and one block's fp32 [block_rows, d] and bf16 [block_rows, d] and
+ * [block_rows, d_ff] buffers.  Zero-filled before first use. */
+size_t ra_bpt_workspace_bytes(const ra_bpt_params_t* p);
+
+/* x [batch, seq_len, d] bf16 (tokens in natural order), out same shape of out_dtype. */
+ra_status_t ra_bpt_fwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_weights_t* w,
+                       void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -143,3 +143,59 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "libra.so"))
     with pytest.raises(RuntimeError, match="not built"):
         api.lib()
+
+
+# ---- blockwise transformer layer: host-side argument checks ------------------------
+
+def test_linear_rejects_bad_arguments(L):
+    ok = (256, 128, 256, FAKE, FAKE, FAKE, None, 0, FAKE, FAKE, 256, None)
+    bad = list(ok)
+    bad[0] = 200                                            # rows % 128
+    assert L.ra_linear(*bad) == 2
+    bad = list(ok)
+    bad[2] = 300                                            # out_features % 256
+    assert L.ra_linear(*bad) == 2
+    bad = list(ok)
+    bad[7] = 2                                              # residual epilogue, no residual
+    assert L.ra_linear(*bad) == 1
+    bad = list(ok)
+    bad[7] = 9
+    assert L.ra_linear(*bad) == 1
+    bad = list(ok)
+    bad[10] = 16                                            # workspace too small
+    assert L.ra_linear(*bad) == 3
+    bad = list(ok)
+    bad[3] = ctypes.c_void_p((1 << 20) + 8)                 # misaligned x
+    assert L.ra_linear(*bad) == 1
+
+
+def test_layernorm_rejects_bad_arguments(L):
+    assert L.ra_layernorm(4, 500, FAKE, FAKE, FAKE, 1e-5, FAKE, 0, None) == 2
+    assert L.ra_layernorm(4, 512, FAKE, FAKE, FAKE, 0.0, FAKE, 0, None) == 1
+    assert L.ra_layernorm(4, 512, FAKE, FAKE, FAKE, 1e-5, FAKE, 5, None) == 1
+    assert L.ra_layernorm(4, 512, None, FAKE, FAKE, 1e-5, FAKE, 0, None) == 1
+
+
+@pytest.mark.parametrize("kw,ok", [
+    (dict(), True),
+    (dict(heads=2), False),                 # d_model 256: not a multiple of 512
+    (dict(d_ff=1000), False),
+    (dict(block_rows=100), False),
+    (dict(kv_heads=2), False),
+    (dict(seq_len=1000), False),            # invalid attention parameters
+])
+def test_bpt_workspace_bytes_validates(L, kw, ok):
+    base = dict(batch=1, seq_len=1024, heads=4, head_dim=128, d_ff=1024, P=4, block=128,
+                block_rows=256, kv_heads=0)
+    base.update(kw)
+    prm = era.make_bpt_params(base["batch"], base["seq_len"], base["heads"], base["head_dim"],
+                              base["d_ff"], base["P"], base["block"], "striped", True,
+                              base["block_rows"])
+    prm.attn.kv_heads = base["kv_heads"]
+    n = era.bpt_workspace_bytes(prm)
+    if ok:
+        d = base["heads"] * base["head_dim"]
+        rows = base["batch"] * base["seq_len"]
+        assert n >= 4 * rows * d * 2 + base["block_rows"] * (d * 6 + base["d_ff"] * 2)
+    else:
+        assert n == 0
