@@ -7,15 +7,19 @@
 //   kEpiBias          out bf16 = acc + bias
 //   kEpiBiasGelu      out bf16 = GELU(acc + bias), GELU(z) = z/2 (1 + erf(z / sqrt 2))
 //   kEpiBiasResidual  out fp32 = acc + bias + residual[M, N] (bf16)
-// One CTA computes one 128 x 256 output tile.  Roles (192 threads):
+// Persistent: one CTA per SM walks output tiles of 128 x 256.  Roles (192 threads):
 //   warp 0      TMA producer: per 64-wide K step one A box (128 x 64) and one B box
-//               (256 x 64), 128-byte swizzled, into a kStages-deep ring
-//   warp 1      TMEM owner (256 columns) and tcgen05.mma issuer: M = 128, N = 256, K = 16
-//               per instruction, both operands K-major from shared memory
+//               (256 x 64), 128-byte swizzled, into a kStages-deep ring shared by all of
+//               the CTA's tiles
+//   warp 1      TMEM owner (512 columns: two 256-column accumulators) and tcgen05.mma
+//               issuer: M = 128, N = 256, K = 16 per instruction, both operands K-major
+//               from shared memory; tile i accumulates in buffer i mod 2
 //   warps 2-5   epilogue, thread = output row = TMEM lane: 32 columns at a time out of
-//               TMEM, bias / GELU / residual in registers, 16-byte stores
-// CTAs walk the M tiles of one N tile before the next, so the resident CTAs share that
-// N tile of B in L2 and A (the activations) is re-read from L2 across N tiles.
+//               TMEM, bias / GELU / residual in registers, 16-byte stores; it releases an
+//               accumulator as soon as it has read it, so a tile's epilogue runs under
+//               the next tile's main loop
+// Tiles are numbered in groups of kGroupM M-tiles (N-tile-major inside a group): the
+// tiles in flight at once share a few row blocks of A and a band of B in L2.
 //
 // LayerNorm: y = (x - mean) / sqrt(var + eps) * gamma + beta per row, var the biased
 // variance, two passes over the row held in registers; 128 threads per row.
@@ -35,7 +39,8 @@ constexpr int kBB = GN * GK * 2;            // B box bytes (32 KB)
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kAB;
 constexpr int kOffBar = kOffB + kStages * kBB;
-constexpr int kNBar = 2 * kStages + 1;      // full[], empty[], acc_full
+constexpr int kNBar = 2 * kStages + 5;      // full[], empty[], acc_full[2], acc_empty[2], drain
+constexpr int kGroupM = 8;                  // M-tiles per raster group
 constexpr int kOffMisc = kOffBar + kNBar * 8;
 constexpr int kGemmSmem = kOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kGemmSmem <= 227 * 1024, "shared memory budget");
@@ -61,6 +66,18 @@ __device__ __forceinline__ float gelu_exact(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
+// Output tile of work item `pid`: groups of kGroupM M-tiles, N-tile-major inside a group,
+// so that the tiles in flight at once (one per SM) share a few M-tiles of A and a band of
+// N-tiles of B in L2.
+__device__ __forceinline__ void tile_of(int pid, int mt, int nt, int& tm, int& tn) {
+  const int per_group = kGroupM * nt;
+  const int first_m = (pid / per_group) * kGroupM;
+  const int gsize = (mt - first_m) < kGroupM ? (mt - first_m) : kGroupM;
+  const int r = pid % per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -72,16 +89,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sB = sm + kOffB;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_full = empty + kStages;      // [2]
+  uint64_t* acc_empty = acc_full + 2;        // [2]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   uint32_t* tmem_slot = misc;
   volatile uint32_t* abort_flag = misc + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int mt = g.M / GM;
-  const int tm = blockIdx.x % mt, tn = blockIdx.x / mt;
-  const int m0 = tm * GM, n0 = tn * GN;
+  const int mt = g.M / GM, nt = g.N / GN;
+  const int ntiles = mt * nt;
   const int nk = g.K / GK;
 
   if (threadIdx.x == 0) {
@@ -90,69 +108,101 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
   __syncthreads();
   if (*abort_flag) return;   // an earlier kernel gave up: uniform early exit
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tacc = *tmem_slot;
+  const uint32_t tbase = *tmem_slot;
   const WaitCtx wc{abort_flag, g.err, g.wait_limit_ns};
 
   if (warp == 0) {
+    // ================================================================ producer =====
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
-      int kb = 0;
-      for (; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, wc)) break;
-        mbar_expect_tx(&full[s], kAB + kBB);
-        tma_load_2d(sA + s * kAB, &tmA, &full[s], kb * GK, m0);
-        tma_load_2d(sB + s * kBB, &tmB, &full[s], kb * GK, n0);
+      int it = 0;                               // K steps issued, over all tiles
+      bool ok = true;
+      for (int pid = blockIdx.x; pid < ntiles && ok; pid += gridDim.x) {
+        int tm, tn;
+        tile_of(pid, mt, nt, tm, tn);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[s], kAB + kBB);
+          tma_load_2d(sA + s * kAB, &tmA, &full[s], kb * GK, tm * GM);
+          tma_load_2d(sB + s * kBB, &tmB, &full[s], kb * GK, tn * GN);
+        }
       }
       // let every copy this thread issued land before the CTA can exit
-      for (int r = (kb > kStages ? kb - kStages : 0); r < kb; ++r)
+      for (int r = (it > kStages ? it - kStages : 0); r < it; ++r)
         wait_drain(&full[r % kStages], (r / kStages) & 1, g.wait_limit_ns);
     }
   } else if (warp == 1) {
+    // ================================================================ MMA issuer ===
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(GM, GN, false, false);
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      int it = 0, lt = 0;
       bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&full[s], (kb / kStages) & 1, wc)) { ok = false; break; }
+      for (int pid = blockIdx.x; pid < ntiles && ok; pid += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t tacc = tbase + buf * GN;
+        // the epilogue has read this accumulator's previous tile out of TMEM
+        if (lt >= 2 && !mbar_wait(&acc_empty[buf], ((lt >> 1) - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        const uint64_t ad = sdesc_kmajor(a0 + s * kAB), bd = sdesc_kmajor(b0 + s * kBB);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&full[s], (it / kStages) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor(a0 + s * kAB), bd = sdesc_kmajor(b0 + s * kBB);
 #pragma unroll
-        for (int kk = 0; kk < GK / 16; ++kk)          // +32 bytes per K step of 16
-          umma_ss(tacc, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&empty[s]);
+          for (int kk = 0; kk < GK / 16; ++kk)        // +32 bytes per K step of 16
+            umma_ss(tacc, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(&acc_full[buf]);
       }
-      umma_commit(acc_full);
-      if (!ok) wait_drain(acc_full, 0, g.wait_limit_ns);
+      umma_commit(drain);
+      wait_drain(drain, 0, g.wait_limit_ns);     // every MMA done before TMEM is released
     }
   } else {
     // ================================================================ epilogue =====
     const int q = warp & 3;                       // TMEM lane quadrant of this warp
     const int r = q * 32 + lane;
-    const size_t row = (size_t)(m0 + r);
-    const uint32_t trow = tacc + (static_cast<uint32_t>(q * 32) << 16);
-    if (mbar_wait(acc_full, 0, wc)) {
+    int lt = 0;
+    for (int pid = blockIdx.x; pid < ntiles; pid += gridDim.x, ++lt) {
+      int tm, tn;
+      tile_of(pid, mt, nt, tm, tn);
+      const int buf = lt & 1;
+      const uint32_t trow = tbase + buf * GN + (static_cast<uint32_t>(q * 32) << 16);
+      const size_t row = (size_t)tm * GM + r;
+      if (!mbar_wait(&acc_full[buf], (lt >> 1) & 1, wc)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < GN / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(trow + 32 * c, v);
         tmem_wait_ld();
-        const int col = n0 + 32 * c;
+        if (c == GN / 32 - 1) {                   // accumulator fully read: release it
+          tc_fence_before();
+          mbar_arrive(&acc_empty[buf]);
+        }
+        const int col = tn * GN + 32 * c;
         float f[32];
         const float4* bias4 = reinterpret_cast<const float4*>(g.bias + col);
 #pragma unroll
@@ -201,7 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tacc, 256);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -266,8 +316,17 @@ __global__ void __launch_bounds__(128)
 
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb, int epi,
                         cudaStream_t s) {
-  const long long grid = (long long)(g.M / GM) * (g.N / GN);
-  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long tiles = (long long)(g.M / GM) * (g.N / GN);
+  if (tiles <= 0 || tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // persistent: one CTA per SM (shared memory allows one), each walking tiles
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      sms = kAutoSplitSMs;
+  }
+  const long long grid = tiles < sms ? tiles : sms;
   cudaError_t e;
   switch (epi) {
     case kEpiBias:
