@@ -158,13 +158,21 @@ def dist_init(args):
 
 
 def dist_max(x, world):
+    """Max of x over the ranks (the slowest rank's time sets the job's time)."""
     if world <= 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(world, flops_per_rank_step, steps, max_ms):
+    """Whole-job TFLOP/s: the useful FLOPs every rank did over the slowest rank's time
+    (every rank runs the same workload on its own GPU: weak scaling)."""
+    return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
 
 
 def dist_barrier(world):
@@ -320,7 +328,7 @@ def run_ours(args, w, rank, world, local):
     f_fwd, f_bwd = flops_of(w)
     step_flops = f_fwd + f_bwd
     ms_per_step = total_ms_max / K
-    value = world * step_flops * K / (total_ms_max * 1e-3) / 1e12
+    value = job_rate(world, step_flops, K, total_ms_max)
     pk, pk_kind = peaks()
     peak_tf = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
@@ -366,7 +374,7 @@ def run_ours(args, w, rank, world, local):
         torch.cuda.synchronize()
         ws.check()
         e_ms = dist_max(a0.elapsed_time(a1), world)
-        e2e = {"value": round(world * step_flops * K / (e_ms * 1e-3) / 1e12, 2),
+        e2e = {"value": round(job_rate(world, step_flops, K, e_ms), 2),
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e_ms / K, 3)}
 
@@ -474,7 +482,7 @@ def run_bpt(args, w, rank, world, local):
     ws.check()
     total_ms = dist_max(t0.elapsed_time(t1), world)
     flops = bpt_flops(w)
-    value = world * flops * K / (total_ms * 1e-3) / 1e12
+    value = job_rate(world, flops, K, total_ms)
 
     # dominant kernel: the feed-forward GEMM of one block (rows br, d -> d_ff, GELU), timed
     # alone with CUDA events on the launching stream
@@ -520,7 +528,7 @@ def run_bpt(args, w, rank, world, local):
         a1.record(stream)
         torch.cuda.synchronize()
         e_ms = dist_max(a0.elapsed_time(a1), world)
-        e2e = {"value": round(world * flops * K / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e = {"value": round(job_rate(world, flops, K, e_ms), 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": ho.numel() * 2,
                "ms_per_step": round(e_ms / K, 3)}
     cpu = None
