@@ -40,7 +40,7 @@ constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kAB;
 constexpr int kOffBar = kOffB + kStages * kBB;
 constexpr int kNBar = 2 * kStages + 5;      // full[], empty[], acc_full[2], acc_empty[2], drain
-constexpr int kGroupM = 8;                  // M-tiles per raster group
+constexpr int kGroupM = 32;                 // M-tiles per raster group
 constexpr int kOffMisc = kOffBar + kNBar * 8;
 constexpr int kGemmSmem = kOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kGemmSmem <= 227 * 1024, "shared memory budget");
