@@ -352,14 +352,22 @@ __global__ void __launch_bounds__(384, 1)
         for (int u = 0; u < ueq; ++u) {
           if (!mbar_wait(&s_full[q], cnt & 1, wc)) { ok = false; break; }
           tc_fence_after();
+          // all four 32-column loads in flight before the one wait
           float sv[128];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tS + 32 * c, r);
+          {
+            uint32_t r0[32], r1[32], r2[32], r3[32];
+            tmem_ld32(tS, r0);
+            tmem_ld32(tS + 32, r1);
+            tmem_ld32(tS + 64, r2);
+            tmem_ld32(tS + 96, r3);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(r[e]);
+            for (int e = 0; e < 32; ++e) {
+              sv[e] = __uint_as_float(r0[e]);
+              sv[32 + e] = __uint_as_float(r1[e]);
+              sv[64 + e] = __uint_as_float(r2[e]);
+              sv[96 + e] = __uint_as_float(r3[e]);
+            }
           }
           if (u == udiag) {
             const int lim = arow - ((a.layout == RA_LAYOUT_STRIPED && j > i) ? 1 : 0);
