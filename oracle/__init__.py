@@ -43,11 +43,12 @@ from .ring import ring_fwd, ring_partials, merge_partials
 from .work import (shard_of, local_of, shard_tokens, ring_order, shard_work,
                    tile_class)
 from .gqa import gqa_fwd, gqa_bwd, group_size
-from .bpt import bpt_layer_fwd, bpt_layer_fwd_blocked, gelu, layer_norm
+from .bpt import bpt_layer_fwd, bpt_layer_fwd_blocked, bpt_layer_rows, gelu, layer_norm
 
 __all__ = [
     "attention_fwd", "attention_bwd", "attention_rows_fwd", "attention_rows_dq", "brute_force_fwd",
     "default_scale", "ring_fwd", "ring_partials", "merge_partials", "shard_of",
     "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class", "gqa_fwd", "gqa_bwd",
-    "group_size", "bpt_layer_fwd", "bpt_layer_fwd_blocked", "gelu", "layer_norm",
+    "group_size", "bpt_layer_fwd", "bpt_layer_fwd_blocked", "bpt_layer_rows", "gelu",
+    "layer_norm",
 ]

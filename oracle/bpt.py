@@ -25,6 +25,9 @@ rest of this package.  Weights follow torch.nn.Linear's layout: W [out_features,
 in_features].  ``bpt_layer_fwd`` computes the whole sequence at once;
 ``bpt_layer_fwd_blocked`` follows the page's loop over query blocks and is used by the
 tests to show that the two agree (the fusion changes memory, not the result).
+``bpt_layer_rows`` evaluates the same definition for a few output rows of a long sequence
+(the keys and values of every earlier row, then the sampled rows only), for checks at
+sizes where the whole layer is out of reach in fp64.
 """
 
 import math
@@ -105,3 +108,24 @@ def bpt_layer_fwd_blocked(x, w, n_heads, causal, block_size):
         ab = np.einsum("bhrc,bchd->brhd", p, v).reshape(B, block_size, d)
         out[:, s:s + block_size] = _post_attention(x[:, s:s + block_size], ab, w)
     return out
+
+
+def bpt_layer_rows(x, w, n_heads, causal, b, rows):
+    """Output rows `rows` of batch entry b of the layer, [len(rows), d]."""
+    B, L, d = x.shape
+    dk = d // n_heads
+    rows = np.asarray(rows)
+    last = int(rows.max()) + 1 if causal else L
+    xb = x[b]
+    kk = linear(xb[:last], w["wk"], w["bk"]).reshape(last, n_heads, dk)
+    vv = linear(xb[:last], w["wv"], w["bv"]).reshape(last, n_heads, dk)
+    qq = linear(xb[rows], w["wq"], w["bq"]).reshape(len(rows), n_heads, dk)
+    a = np.zeros((len(rows), n_heads, dk))
+    for n, r in enumerate(rows):
+        c = int(r) + 1 if causal else L
+        s = np.einsum("hd,chd->hc", qq[n], kk[:c]) / math.sqrt(dk)
+        s -= s.max(axis=-1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=-1, keepdims=True)
+        a[n] = np.einsum("hc,chd->hd", p, vv[:c])
+    return _post_attention(xb[rows], a.reshape(len(rows), d), w)

@@ -98,3 +98,25 @@ def test_bpt_blocking_does_not_change_the_result():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     got = _f64(outs[0])
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-2
+
+
+def test_bpt_fullsize_sampled_rows():
+    """The 32k layer workload in the configuration bench.py times (zigzag, block_rows
+    16384, bf16 output), checked on sampled rows: both ends, the block boundary, interior
+    rows.  The oracle computes K and V of every row and the layer for the sampled rows."""
+    from exact_blockwise_ring_gb300.synthetic import WORKLOADS, SEEDS
+    wl = WORKLOADS["32k-bpt"]
+    B, L, H, D, P, blk = (wl["batch"], wl["seq_len"], wl["heads"], wl["head_dim"], wl["P"],
+                          wl["block"])
+    d, d_ff, br = H * D, wl["d_ff"], wl["block_rows"]
+    x = make_inputs(B, L, 1, d, SEEDS["32k-bpt"], with_dout=False)[0].view(B, L, d)
+    w = make_bpt_weights(d, d_ff, SEEDS["32k-bpt"] + 1)
+    out = era.ra_bpt_fwd(x.cuda(), {k: v.cuda() for k, v in w.items()}, H, P, blk, "zigzag",
+                         True, block_rows=br)
+    torch.cuda.synchronize()
+    rows = [0, 1, br - 1, br, L // 3 + 7, L - 1]
+    ref = oracle.bpt_layer_rows(_f64(x), {k: _f64(v) for k, v in w.items()}, H, True, 0, rows)
+    got = _f64(out[0, rows])
+    err = got - ref
+    assert np.linalg.norm(err) / np.linalg.norm(ref) <= 1e-2
+    assert np.all(np.abs(err) <= 5e-2 + 2.0 ** -8 * np.abs(ref))

@@ -84,6 +84,17 @@ def test_blockwise_loop_equals_whole_sequence(causal, block):
     assert np.max(np.abs(a - b)) < 1e-11
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_sampled_rows_equal_the_whole_layer(causal):
+    w = _weights(64, 128, seed=8)
+    x = np.random.default_rng(9).standard_normal((2, 96, 64))
+    full = oracle.bpt_layer_fwd(x, w, 2, causal)
+    rows = [0, 1, 37, 95]
+    for b in range(2):
+        got = oracle.bpt_layer_rows(x, w, 2, causal, b, rows)
+        assert np.max(np.abs(got - full[b, rows])) < 1e-11
+
+
 def test_gelu_is_z_times_normal_cdf():
     z = np.array([-3.0, -1.0, 0.0, 0.5, 1.0, 2.0, 6.0])
     # Phi(1) and Phi(-1) to 16 digits, Phi(0) = 1/2
