@@ -87,6 +87,20 @@ def test_bpt_layer_parity(layout):
     assert np.max(np.abs(err)) <= 5e-2
 
 
+def test_bpt_layer_noncausal_contiguous():
+    B, L, H, d_ff, P = 2, 512, 4, 512, 2
+    d = H * 128
+    x = make_inputs(B, L, 1, d, 70, with_dout=False)[0].view(B, L, d)
+    w = make_bpt_weights(d, d_ff, 71)
+    ref = oracle.bpt_layer_fwd(_f64(x), {k: _f64(v) for k, v in w.items()}, H, False)
+    out = era.ra_bpt_fwd(x.cuda(), {k: v.cuda() for k, v in w.items()}, H, P, 128, "contiguous",
+                         False, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    err = _f64(out) - ref
+    assert np.linalg.norm(err) / np.linalg.norm(ref) <= 1e-2
+    assert np.max(np.abs(err)) <= 5e-2
+
+
 def test_bpt_blocking_does_not_change_the_result():
     B, L, H, d_ff, P = 2, 1024, 4, 512, 4
     x, w, ref = _layer_case(B, L, H, d_ff, seed=60)

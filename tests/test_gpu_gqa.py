@@ -85,3 +85,17 @@ def test_gqa_rejects_non_dividing_kv_heads():
                                              kv_heads=4))
     with pytest.raises(ValueError):
         era.ra_fwd(q, k, v, 4, 128, "striped", True)
+
+
+@pytest.mark.parametrize("D,n_split,layout", [(128, 2, "striped"), (64, 1, "zigzag"),
+                                              (64, 4, "contiguous")])
+def test_gqa_forward_split_and_head_dim_64(D, n_split, layout):
+    B, L, H, Hkv, P = 1, 2048, 8, 2, 4
+    q, k, v = make_inputs(B, L, H, D, seed=90 + D + n_split, with_dout=False, kv_heads=Hkv)
+    q64, k64, v64 = to_f64(q, k, v)
+    o_ref, l_ref = oracle.gqa_fwd(q64, k64, v64, True)
+    o, l = era.ra_fwd(q.cuda(), k.cuda(), v.cuda(), P, 128, layout, True,
+                      out_dtype=torch.float32, n_split=n_split)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(o.cpu().numpy() - o_ref)) <= OUT_TOL
+    assert np.max(np.abs(l.cpu().numpy() - l_ref)) <= LSE_TOL

@@ -36,19 +36,20 @@ def _rel(a, b):
     return float((a - b).norm() / b.norm())
 
 
-def test_noalloc_backward_matches_workspace_backward_twice():
+@pytest.mark.parametrize("layout,Hkv", [("striped", 4), ("zigzag", 2)])
+def test_noalloc_backward_matches_workspace_backward_twice(layout, Hkv):
     torch.cuda.init()
-    B, L, H, D, P, block, layout = 1, 2048, 4, 128, 4, 128, "striped"
-    q, k, v, do = (t.cuda() for t in make_inputs(B, L, H, D, seed=77))
+    B, L, H, D, P, block = 1, 2048, 4, 128, 4, 128
+    q, k, v, do = (t.cuda() for t in make_inputs(B, L, H, D, seed=77, kv_heads=Hkv))
     out, lse = era.ra_fwd(q, k, v, P, block, layout, True)
     ref = era.ra_bwd(q, k, v, out, lse, do, P, block, layout, True)
     torch.cuda.synchronize()
     f = _noalloc()
-    prm = api.make_params(B, L, H, D, P, block, layout, True)
+    prm = api.make_params(B, L, H, D, P, block, layout, True, kv_heads=Hkv)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
         # poison the outputs so a call that wrote nothing cannot pass
-        dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+        dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
         st = f(ctypes.byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), 0,
                lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), stream)
         assert st == 0, api.lib().ra_last_error_message()
