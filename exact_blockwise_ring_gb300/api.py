@@ -283,14 +283,31 @@ def ra_selftest_timeout(workspace, timeout_us, stream=None):
     _check(lib().ra_selftest_timeout(_ptr(buf), buf.numel(), int(timeout_us), _stream(stream)))
 
 
+def _want(t, dtype, name, shape=None, device=None):
+    """Raise unless t is a contiguous CUDA tensor of dtype (and shape / device)."""
+    if t is None or not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if device is not None and t.device != device:
+        raise ValueError("%s must be on %s" % (name, device))
+
+
 def ra_linear(x, weight, bias, epilogue="bias", residual=None, workspace=None, stream=None,
               out=None):
     """out = epilogue(x weight^T + bias) through ra_linear.  x [..., in] bf16, weight
     [out, in] bf16, bias [out] fp32; "bias" / "bias_gelu" give bf16, "bias_residual" adds
     residual [..., out] bf16 and gives fp32."""
     epi = EPILOGUES[epilogue]
-    rows = x.numel() // x.shape[-1]
     n_out, n_in = weight.shape
+    _want(x, torch.bfloat16, "x")
+    _want(weight, torch.bfloat16, "weight")
+    _want(bias, torch.float32, "bias", (n_out,))
+    if x.shape[-1] != n_in:
+        raise ValueError("x has %d features, weight expects %d" % (x.shape[-1], n_in))
+    if epi == 2:
+        _want(residual, torch.bfloat16, "residual", tuple(x.shape[:-1]) + (n_out,))
+    rows = x.numel() // x.shape[-1]
     shape = tuple(x.shape[:-1]) + (n_out,)
     if out is None:
         out = torch.empty(shape, dtype=torch.float32 if epi == 2 else torch.bfloat16,
@@ -305,6 +322,9 @@ def ra_linear(x, weight, bias, epilogue="bias", residual=None, workspace=None, s
 def ra_layernorm(x, gamma, beta, eps=1e-5, out_dtype=torch.bfloat16, stream=None):
     """LayerNorm over the last dimension of fp32 x through ra_layernorm."""
     d = x.shape[-1]
+    _want(x, torch.float32, "x")
+    _want(gamma, torch.float32, "gamma", (d,))
+    _want(beta, torch.float32, "beta", (d,))
     out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
     odt = RA_FP32 if out_dtype == torch.float32 else RA_BF16
     _check(lib().ra_layernorm(x.numel() // d, d, _ptr(x), _ptr(gamma), _ptr(beta), float(eps),
@@ -327,7 +347,16 @@ def ra_bpt_fwd(x, weights, heads, P, block, layout="contiguous", causal=True, bl
     """One blockwise transformer layer forward through ra_bpt_fwd.  x [B, L, d] bf16;
     weights: dict with the names of BPT_WEIGHTS (weights bf16 [out, in], the rest fp32)."""
     B, L, d = x.shape
+    _want(x, torch.bfloat16, "x")
     d_ff = weights["w1"].shape[0]
+    shapes = {"wq": (d, d), "wk": (d, d), "wv": (d, d), "wo": (d, d), "w1": (d_ff, d),
+              "w2": (d, d_ff), "bq": (d,), "bk": (d,), "bv": (d,), "bo": (d,), "b1": (d_ff,),
+              "b2": (d,), "ln1_g": (d,), "ln1_b": (d,), "ln2_g": (d,), "ln2_b": (d,)}
+    for n in BPT_WEIGHTS:
+        if n not in weights:
+            raise ValueError("missing layer parameter %r" % n)
+        _want(weights[n], torch.bfloat16 if n[0] == "w" else torch.float32, n, shapes[n],
+              x.device)
     prm = make_bpt_params(B, L, heads, d // heads, d_ff, P, block, layout, causal, block_rows)
     w = BptWeights(*[weights[n].data_ptr() for n in BPT_WEIGHTS])
     if out is None:

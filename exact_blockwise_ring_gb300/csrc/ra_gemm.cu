@@ -318,14 +318,11 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensor
                         cudaStream_t s) {
   const long long tiles = (long long)(g.M / GM) * (g.N / GN);
   if (tiles <= 0 || tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  // persistent: one CTA per SM (shared memory allows one), each walking tiles
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-      sms = kAutoSplitSMs;
-  }
+  // persistent: one CTA per SM of the current device (shared memory allows one)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = kAutoSplitSMs;
   const long long grid = tiles < sms ? tiles : sms;
   cudaError_t e;
   switch (epi) {

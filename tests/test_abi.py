@@ -199,3 +199,16 @@ def test_bpt_workspace_bytes_validates(L, kw, ok):
         assert n >= 4 * rows * d * 2 + base["block_rows"] * (d * 6 + base["d_ff"] * 2)
     else:
         assert n == 0
+
+
+def test_layer_bindings_check_their_inputs_before_any_call():
+    import torch
+    x = torch.zeros((128, 64), dtype=torch.bfloat16)          # a CPU tensor: refused
+    w = torch.zeros((256, 64), dtype=torch.bfloat16)
+    b = torch.zeros(256)
+    with pytest.raises(ValueError, match="CUDA"):
+        era.ra_linear(x, w, b)
+    with pytest.raises(ValueError, match="CUDA"):
+        era.ra_layernorm(torch.zeros((4, 512)), torch.ones(512), torch.zeros(512))
+    with pytest.raises(ValueError, match="CUDA"):
+        era.ra_bpt_fwd(torch.zeros((1, 1024, 512), dtype=torch.bfloat16), {}, 4, 4, 128)
