@@ -209,7 +209,29 @@ def cpu_baseline(w):
     return {"value": tf / t, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": "fp64 oracle fwd+bwd, 1 head x %d tokens (causal) of the workload's "
                       "input distribution, %.1f s; useful-FLOP convention of the GPU line"
-                      % (CPU_SAMPLE_TOKENS, t)}
+                      % (CPU_SAMPLE_TOKENS, t),
+            "one_thread": oracle_one_thread()}
+
+
+def oracle_one_thread():
+    """The oracle with its BLAS on one thread (a child process with the thread-count
+    variables set before NumPy loads), on one head of the tiny and the 8k workloads."""
+    code = ("import json, sys, bench; w = bench.workload(sys.argv[1], None); "
+            "t, tf, c = bench.oracle_sample(w, w['seq_len']); print(json.dumps([t, tf]))")
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+              "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    res = {}
+    for name in ("tiny", "8k"):
+        try:
+            r = subprocess.run([sys.executable, "-c", code, name], cwd=ROOT, env=env,
+                               capture_output=True, text=True, timeout=300)
+            t, tf = json.loads(r.stdout.strip().splitlines()[-1])
+            res[name] = {"tflops": tf / t, "seconds": round(t, 3)}
+        except Exception as e:          # a report field: never fails the bench
+            res[name] = {"error": str(e)[:120]}
+    return res
 
 
 def source_hash(*names):
@@ -423,6 +445,19 @@ def run_ours(args, w, rank, world, local):
     if not args.no_merge:
         hbm_kernels["merge_kernel"] = time_merge(era, B, L, H, D, dev, stream, hbm)
 
+    # the secondary ceiling: one exp per unmasked pair in the forward and one in the
+    # backward, against the measured MUFU rate (about 31 exp2 per clock per SM on this part)
+    # at the median SM clock seen
+    pairs = B * H * pairs_of(L, causal)
+    mhz = (clk or {}).get("sm_mhz") or 2070.0
+    ceil = 31.0 * 152 * mhz * 1e6
+    mufu = {"exp_per_s_fwd": round(pairs / (fwd_ms * 1e-3), 0),
+            "exp_per_s_bwd": round(pairs / (main_ms * 1e-3), 0),
+            "ceiling_exp_per_s": round(ceil, 0),
+            "frac_fwd": round(pairs / (fwd_ms * 1e-3) / ceil, 4),
+            "frac_bwd": round(pairs / (main_ms * 1e-3) / ceil, 4),
+            "ceiling_kind": "31 exp2/clk/SM (microbenchmark on this part) x 152 SMs x median SM clock"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
@@ -438,7 +473,8 @@ def run_ours(args, w, rank, world, local):
                              "bwd_main": round(main_ms, 3), "bwd_finalize": round(fin_ms, 3)},
                 "roofline": roofline, "hbm_kernels": hbm_kernels, "cpu_baseline": cpu,
                 "e2e": e2e,
-                "gpu_launches": 4 * K, "clocks": clk}
+                "tflops_12d": round(value * 12.0 / 14.0, 2),
+                "mufu": mufu, "gpu_launches": 4 * K, "clocks": clk}
         print(json.dumps(line), flush=True)
 
 
