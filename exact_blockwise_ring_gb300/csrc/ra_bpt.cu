@@ -38,25 +38,38 @@ ra_status_t check_linear(int64_t rows, int in_f, int out_f, int epi) {
   return RA_OK;
 }
 
-ra_status_t run_linear(int64_t rows, int in_f, int out_f, const void* x, const void* weight,
-                       const float* bias, const void* residual, int epi, void* out,
-                       unsigned int* err, cudaStream_t st) {
+// out[M, N] = epilogue(A B): A stored [M, K] (a_mn = 0) or [K, M] (a_mn = 1), B stored
+// [N, K] (b_mn = 0) or [K, N] (b_mn = 1); shapes already checked.
+ra_status_t run_gemm(int64_t M, int N, int K, const void* a, int a_mn, const void* b, int b_mn,
+                     const float* bias, const void* aux, int epi, void* out, unsigned int* err,
+                     cudaStream_t st) {
   CUtensorMap ta, tb;
   ra_status_t s;
-  if ((s = encode_2d_bf16(&ta, x, in_f, rows, 64, 128)) != RA_OK) return s;
-  if ((s = encode_2d_bf16(&tb, weight, in_f, out_f, 64, 256)) != RA_OK) return s;
+  if (a_mn) s = encode_2d_bf16(&ta, a, M, K, 64, 64);
+  else s = encode_2d_bf16(&ta, a, K, M, 64, 128);
+  if (s != RA_OK) return s;
+  if (b_mn) s = encode_2d_bf16(&tb, b, N, K, 64, 64);
+  else s = encode_2d_bf16(&tb, b, K, N, 64, 256);
+  if (s != RA_OK) return s;
   GemmArgs g{};
-  g.M = (int)rows;
-  g.N = out_f;
-  g.K = in_f;
+  g.M = (int)M;
+  g.N = N;
+  g.K = K;
   g.bias = bias;
-  g.residual = residual;
+  g.aux = aux;
   g.out = out;
   g.err = err;
   g.wait_limit_ns = kWaitLimitNs;
-  cudaError_t e = launch_gemm(g, ta, tb, epi, st);
+  cudaError_t e = launch_gemm(g, ta, tb, epi, a_mn, b_mn, st);
   if (e != cudaSuccess) return bfail(RA_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return RA_OK;
+}
+
+// y = x W^T + b (and its fused epilogue): A = x [rows, in], B = W [out, in], both K-major.
+ra_status_t run_linear(int64_t rows, int in_f, int out_f, const void* x, const void* weight,
+                       const float* bias, const void* residual, int epi, void* out,
+                       unsigned int* err, cudaStream_t st) {
+  return run_gemm(rows, out_f, in_f, x, 0, weight, 0, bias, residual, epi, out, err, st);
 }
 
 // Workspace layout of ra_bpt_fwd (offsets from the base, each 256-byte aligned).

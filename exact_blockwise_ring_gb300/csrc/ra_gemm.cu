@@ -66,6 +66,22 @@ __device__ __forceinline__ float gelu_exact(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
+// d GELU / dz = Phi(z) + z phi(z)
+__device__ __forceinline__ float gelu_grad(float z) {
+  return 0.5f * (1.0f + erff(z * 0.70710678118654752f)) +
+         z * 0.39894228040143268f * __expf(-0.5f * z * z);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* f) {
+  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[x]));
+    f[2 * x] = p.x;
+    f[2 * x + 1] = p.y;
+  }
+}
+
 // Output tile of work item `pid`: groups of kGroupM M-tiles, N-tile-major inside a group,
 // so that the tiles in flight at once (one per SM) share a few M-tiles of A and a band of
 // N-tiles of B in L2.
@@ -78,7 +94,7 @@ __device__ __forceinline__ void tile_of(int pid, int mt, int nt, int& tm, int& t
   tn = r / gsize;
 }
 
-template <int EPI>
+template <int EPI, int A_MN, int B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
@@ -144,8 +160,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           mbar_expect_tx(&full[s], kAB + kBB);
-          tma_load_2d(sA + s * kAB, &tmA, &full[s], kb * GK, tm * GM);
-          tma_load_2d(sB + s * kBB, &tmB, &full[s], kb * GK, tn * GN);
+          // K-major: one box of rows x 64 K; MN-major: boxes of 64 K rows x 64 M (or N)
+          if (A_MN) {
+#pragma unroll
+            for (int b4 = 0; b4 < GM / 64; ++b4)
+              tma_load_2d(sA + s * kAB + b4 * 8192, &tmA, &full[s], tm * GM + 64 * b4, kb * GK);
+          } else {
+            tma_load_2d(sA + s * kAB, &tmA, &full[s], kb * GK, tm * GM);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int b4 = 0; b4 < GN / 64; ++b4)
+              tma_load_2d(sB + s * kBB + b4 * 8192, &tmB, &full[s], tn * GN + 64 * b4, kb * GK);
+          } else {
+            tma_load_2d(sB + s * kBB, &tmB, &full[s], kb * GK, tn * GN);
+          }
         }
       }
       // let every copy this thread issued land before the CTA can exit
@@ -155,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ================================================================ MMA issuer ===
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(GM, GN, false, false);
+      constexpr uint32_t idesc = idesc_bf16(GM, GN, A_MN != 0, B_MN != 0);
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
       int it = 0, lt = 0;
       bool ok = true;
@@ -169,10 +198,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int s = it % kStages;
           if (!mbar_wait(&full[s], (it / kStages) & 1, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t ad = sdesc_kmajor(a0 + s * kAB), bd = sdesc_kmajor(b0 + s * kBB);
+          // K-major: +32 bytes per K step of 16; MN-major: +16 rows of 128 bytes, with the
+          // 64-wide M (N) blocks 8 KB apart
+          const uint64_t ad = A_MN ? sdesc_mnmajor(a0 + s * kAB, 8192) : sdesc_kmajor(a0 + s * kAB);
+          const uint64_t bd = B_MN ? sdesc_mnmajor(b0 + s * kBB, 8192) : sdesc_kmajor(b0 + s * kBB);
 #pragma unroll
-          for (int kk = 0; kk < GK / 16; ++kk)        // +32 bytes per K step of 16
-            umma_ss(tacc, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < GK / 16; ++kk)
+            umma_ss(tacc, ad + (A_MN ? 128 : 2) * kk, bd + (B_MN ? 128 : 2) * kk, idesc,
+                    (kb > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&empty[s]);
         }
         if (ok) umma_commit(&acc_full[buf]);
@@ -203,40 +236,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive(&acc_empty[buf]);
         }
         const int col = tn * GN + 32 * c;
+        const size_t e0 = row * g.N + col;
         float f[32];
-        const float4* bias4 = reinterpret_cast<const float4*>(g.bias + col);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 bb = __ldg(bias4 + e);
-          f[4 * e + 0] = __uint_as_float(v[4 * e + 0]) + bb.x;
-          f[4 * e + 1] = __uint_as_float(v[4 * e + 1]) + bb.y;
-          f[4 * e + 2] = __uint_as_float(v[4 * e + 2]) + bb.z;
-          f[4 * e + 3] = __uint_as_float(v[4 * e + 3]) + bb.w;
+        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);
+        if (EPI == kEpiBias || EPI == kEpiBiasGelu || EPI == kEpiBiasResidual) {
+          const float4* bias4 = reinterpret_cast<const float4*>(g.bias + col);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 bb = __ldg(bias4 + e);
+            f[4 * e + 0] += bb.x;
+            f[4 * e + 1] += bb.y;
+            f[4 * e + 2] += bb.z;
+            f[4 * e + 3] += bb.w;
+          }
         }
-        if (EPI == kEpiBiasResidual) {
-          const uint4* res = reinterpret_cast<const uint4*>(
-              reinterpret_cast<const __nv_bfloat16*>(g.residual) + row * g.N + col);
-          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + row * g.N + col);
+        if (EPI == kEpiBiasGelu) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = gelu_exact(f[e]);
+        }
+        if (EPI == kEpiBiasResidual || EPI == kEpiGeluGrad) {
+          // bf16 [M, N] operand: the residual, or the GELU's input z
+          const uint4* aux = reinterpret_cast<const uint4*>(
+              reinterpret_cast<const __nv_bfloat16*>(g.aux) + e0);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint4 w = __ldg(res + e);
-            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+            float z[8];
+            bf16x8_to_f32(__ldg(aux + e), z);
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[x]));
-              f[8 * e + 2 * x] += p.x;
-              f[8 * e + 2 * x + 1] += p.y;
-            }
+            for (int x = 0; x < 8; ++x)
+              f[8 * e + x] = (EPI == kEpiGeluGrad) ? f[8 * e + x] * gelu_grad(z[x])
+                                                   : f[8 * e + x] + z[x];
           }
+        }
+        if (EPI == kEpiAddF32) {
+          // add the fp32 operand and store, 4 columns at a time
+          const float4* aux = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g.aux) + e0);
+          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + e0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 r4 = __ldg(aux + e);
+            o[e] = make_float4(f[4 * e] + r4.x, f[4 * e + 1] + r4.y, f[4 * e + 2] + r4.z,
+                               f[4 * e + 3] + r4.w);
+          }
+        } else if (EPI == kEpiBiasResidual || EPI == kEpiPlainF32) {
+          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + e0);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             o[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
         } else {
-          if (EPI == kEpiBiasGelu) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) f[e] = gelu_exact(f[e]);
-          }
-          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(g.out) + row * g.N + col);
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(g.out) + e0);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             o[e] = make_uint4(pack_bf16x2(f[8 * e], f[8 * e + 1]), pack_bf16x2(f[8 * e + 2], f[8 * e + 3]),
@@ -314,8 +363,31 @@ __global__ void __launch_bounds__(128)
 
 }  // namespace
 
+namespace {
+
+template <int EPI, int A_MN, int B_MN>
+cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb,
+                       unsigned grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI, A_MN, B_MN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  gemm_kernel<EPI, A_MN, B_MN><<<grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_supported(int epi, int a_mn, int b_mn) {
+  if (!a_mn && !b_mn) return epi >= kEpiBias && epi <= kEpiPlainBf16;
+  if (!a_mn && b_mn)
+    return epi == kEpiPlainF32 || epi == kEpiGeluGrad || epi == kEpiAddF32 || epi == kEpiPlainBf16;
+  if (a_mn && b_mn) return epi == kEpiPlainF32;
+  return false;
+}
+
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb, int epi,
-                        cudaStream_t s) {
+                        int a_mn, int b_mn, cudaStream_t s) {
+  if (!gemm_supported(epi, a_mn, b_mn)) return cudaErrorInvalidValue;
   const long long tiles = (long long)(g.M / GM) * (g.N / GN);
   if (tiles <= 0 || tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM of the current device (shared memory allows one)
@@ -323,31 +395,27 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensor
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     sms = kAutoSplitSMs;
-  const long long grid = tiles < sms ? tiles : sms;
-  cudaError_t e;
-  switch (epi) {
-    case kEpiBias:
-      e = cudaFuncSetAttribute(gemm_kernel<kEpiBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kGemmSmem);
-      if (e != cudaSuccess) return e;
-      gemm_kernel<kEpiBias><<<(unsigned)grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, g);
-      break;
-    case kEpiBiasGelu:
-      e = cudaFuncSetAttribute(gemm_kernel<kEpiBiasGelu>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-      if (e != cudaSuccess) return e;
-      gemm_kernel<kEpiBiasGelu><<<(unsigned)grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, g);
-      break;
-    case kEpiBiasResidual:
-      e = cudaFuncSetAttribute(gemm_kernel<kEpiBiasResidual>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-      if (e != cudaSuccess) return e;
-      gemm_kernel<kEpiBiasResidual><<<(unsigned)grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, g);
-      break;
-    default:
-      return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  if (!a_mn && !b_mn) {
+    switch (epi) {
+      case kEpiBias: return launch_one<kEpiBias, 0, 0>(g, ta, tb, grid, s);
+      case kEpiBiasGelu: return launch_one<kEpiBiasGelu, 0, 0>(g, ta, tb, grid, s);
+      case kEpiBiasResidual: return launch_one<kEpiBiasResidual, 0, 0>(g, ta, tb, grid, s);
+      case kEpiPlainF32: return launch_one<kEpiPlainF32, 0, 0>(g, ta, tb, grid, s);
+      case kEpiGeluGrad: return launch_one<kEpiGeluGrad, 0, 0>(g, ta, tb, grid, s);
+      case kEpiAddF32: return launch_one<kEpiAddF32, 0, 0>(g, ta, tb, grid, s);
+      default: return launch_one<kEpiPlainBf16, 0, 0>(g, ta, tb, grid, s);
+    }
   }
-  return cudaGetLastError();
+  if (!a_mn) {
+    switch (epi) {
+      case kEpiPlainF32: return launch_one<kEpiPlainF32, 0, 1>(g, ta, tb, grid, s);
+      case kEpiGeluGrad: return launch_one<kEpiGeluGrad, 0, 1>(g, ta, tb, grid, s);
+      case kEpiAddF32: return launch_one<kEpiAddF32, 0, 1>(g, ta, tb, grid, s);
+      default: return launch_one<kEpiPlainBf16, 0, 1>(g, ta, tb, grid, s);
+    }
+  }
+  return launch_one<kEpiPlainF32, 1, 1>(g, ta, tb, grid, s);
 }
 
 cudaError_t launch_layernorm(const float* x, const float* gamma, const float* beta, float eps,

@@ -164,19 +164,35 @@ struct BwdArgs {
 };
 
 // Dense kernels of the blockwise transformer layer (ra_gemm.cu).
-enum GemmEpilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResidual = 2 };
+// Epilogues (out[M, N] from the fp32 accumulator acc):
+//   kEpiBias          bf16  acc + bias
+//   kEpiBiasGelu      bf16  GELU(acc + bias)
+//   kEpiBiasResidual  fp32  acc + bias + aux (bf16 [M, N])
+//   kEpiPlainF32      fp32  acc
+//   kEpiGeluGrad      bf16  acc * GELU'(aux), aux = the GELU's input z (bf16 [M, N])
+//   kEpiAddF32        fp32  acc + aux (fp32 [M, N])
+//   kEpiPlainBf16     bf16  acc
+enum GemmEpilogue : int {
+  kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResidual = 2, kEpiPlainF32 = 3, kEpiGeluGrad = 4,
+  kEpiAddF32 = 5, kEpiPlainBf16 = 6
+};
 
+// out[M, N] = epilogue(sum_k A[m, k] B[n, k]); M % 128, N % 256, K % 64 == 0.  A is read
+// K-major (stored [M, K]) or, with a_mn, MN-major (stored [K, M]); B likewise ([N, K] or
+// [K, N]).  Supported: (a_mn, b_mn) = (0, 0) with every epilogue, (0, 1) with kEpiPlainF32,
+// kEpiGeluGrad, kEpiAddF32, kEpiPlainBf16, and (1, 1) with kEpiPlainF32.
 struct GemmArgs {
-  int M, N, K;              // out[M, N] = A[M, K] B[N, K]^T; M % 128, N % 256, K % 64 == 0
-  const float* bias;        // [N] fp32
-  const void* residual;     // [M, N] bf16 (kEpiBiasResidual)
-  void* out;                // [M, N] bf16, or fp32 for kEpiBiasResidual
+  int M, N, K;
+  const float* bias;        // [N] fp32 (kEpiBias, kEpiBiasGelu, kEpiBiasResidual)
+  const void* aux;          // [M, N] operand of kEpiBiasResidual, kEpiGeluGrad, kEpiAddF32
+  void* out;
   unsigned int* err;        // workspace error word
   uint64_t wait_limit_ns;
 };
 
+bool gemm_supported(int epi, int a_mn, int b_mn);
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb, int epi,
-                        cudaStream_t s);
+                        int a_mn, int b_mn, cudaStream_t s);
 cudaError_t launch_layernorm(const float* x, const float* gamma, const float* beta, float eps,
                              long long rows, int d, void* out, int out_fp32, cudaStream_t s);
 

@@ -30,7 +30,8 @@ Modules:
     gqa       -- grouped-query attention (fewer key/value heads than query heads) on top
                  of ``attention``.
     bpt       -- one Blockwise Parallel Transformer layer (projections, attention, output
-                 projection, residuals, LayerNorms, GELU feed-forward), forward.
+                 projection, residuals, LayerNorms, GELU feed-forward), forward and
+                 backward.
 
 Parity status: every function here is pinned by tests in ``tests/test_oracle_*.py``
 against things other than itself (a library softmax attention, closed forms,
@@ -43,12 +44,13 @@ from .ring import ring_fwd, ring_partials, merge_partials
 from .work import (shard_of, local_of, shard_tokens, ring_order, shard_work,
                    tile_class)
 from .gqa import gqa_fwd, gqa_bwd, group_size
-from .bpt import bpt_layer_fwd, bpt_layer_fwd_blocked, bpt_layer_rows, gelu, layer_norm
+from .bpt import (bpt_layer_bwd, bpt_layer_fwd, bpt_layer_fwd_blocked, bpt_layer_rows, gelu,
+                  gelu_grad, layer_norm, layer_norm_bwd)
 
 __all__ = [
     "attention_fwd", "attention_bwd", "attention_rows_fwd", "attention_rows_dq", "brute_force_fwd",
     "default_scale", "ring_fwd", "ring_partials", "merge_partials", "shard_of",
     "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class", "gqa_fwd", "gqa_bwd",
-    "group_size", "bpt_layer_fwd", "bpt_layer_fwd_blocked", "bpt_layer_rows", "gelu",
-    "layer_norm",
+    "group_size", "bpt_layer_fwd", "bpt_layer_fwd_blocked", "bpt_layer_rows", "bpt_layer_bwd",
+    "gelu", "gelu_grad", "layer_norm", "layer_norm_bwd",
 ]

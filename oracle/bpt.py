@@ -1,4 +1,4 @@
-"""One Blockwise Parallel Transformer layer, forward, in fp64.
+"""One Blockwise Parallel Transformer layer, forward and backward, in fp64.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
@@ -27,7 +27,13 @@ in_features].  ``bpt_layer_fwd`` computes the whole sequence at once;
 tests to show that the two agree (the fusion changes memory, not the result).
 ``bpt_layer_rows`` evaluates the same definition for a few output rows of a long sequence
 (the keys and values of every earlier row, then the sampled rows only), for checks at
-sizes where the whole layer is out of reach in fp64.
+sizes where the whole layer is out of reach in fp64.  ``bpt_layer_bwd`` gives the gradients
+of sum(out * dout) with respect to x and every parameter by the chain rule through the
+steps above (the attention's own backward is ``attention_bwd``):
+    LN backward: dy = rstd (dyh - mean(dyh) - yh mean(dyh yh)), dyh = dout g,
+                 dg = sum dout yh, db = sum dout;
+    Linear backward: dx = dy W, dW = dy^T x, db = sum dy;
+    GELU backward: dz = df (Phi(z) + z phi(z)).
 """
 
 import math
@@ -129,3 +135,59 @@ def bpt_layer_rows(x, w, n_heads, causal, b, rows):
         p /= p.sum(axis=-1, keepdims=True)
         a[n] = np.einsum("hc,chd->hd", p, vv[:c])
     return _post_attention(xb[rows], a.reshape(len(rows), d), w)
+
+
+def gelu_grad(z):
+    """d GELU / dz = Phi(z) + z phi(z)."""
+    return 0.5 * (1.0 + _erf(z / math.sqrt(2.0))) + z * np.exp(-0.5 * z * z) / math.sqrt(2 * math.pi)
+
+
+def layer_norm_bwd(y, g, dout, eps=LN_EPS):
+    """Gradients of LN(y) = (y - mean) / sqrt(var + eps) * g + b over the last axis:
+    returns (dy, dg, db) with dg, db summed over every leading axis."""
+    mu = y.mean(axis=-1, keepdims=True)
+    rstd = 1.0 / np.sqrt(((y - mu) ** 2).mean(axis=-1, keepdims=True) + eps)
+    yh = (y - mu) * rstd
+    dyh = dout * g
+    dy = rstd * (dyh - dyh.mean(axis=-1, keepdims=True) - yh * (dyh * yh).mean(axis=-1, keepdims=True))
+    lead = tuple(range(y.ndim - 1))
+    return dy, (dout * yh).sum(axis=lead), dout.sum(axis=lead)
+
+
+def _linear_bwd(xin, w, dy):
+    """y = xin w^T + b: returns (dxin, dw, db) with the rows of every leading axis summed."""
+    d2 = dy.reshape(-1, dy.shape[-1])
+    x2 = xin.reshape(-1, xin.shape[-1])
+    return dy @ w, d2.T @ x2, d2.sum(axis=0)
+
+
+def bpt_layer_bwd(x, w, n_heads, causal, dout):
+    """Gradients of sum(out * dout) for the layer of bpt_layer_fwd, by the chain rule:
+    returns a dict with "x" and every name of WEIGHT_NAMES."""
+    from .attention import attention_bwd
+    B, L, d = x.shape
+    q = _heads(linear(x, w["wq"], w["bq"]), n_heads)
+    k = _heads(linear(x, w["wk"], w["bk"]), n_heads)
+    v = _heads(linear(x, w["wv"], w["bv"]), n_heads)
+    a4, _ = attention_fwd(q, k, v, causal)
+    a = a4.reshape(B, L, d)
+    y1 = x + linear(a, w["wo"], w["bo"])
+    h1 = layer_norm(y1, w["ln1_g"], w["ln1_b"])
+    z = linear(h1, w["w1"], w["b1"])
+    f = gelu(z)
+    y2 = h1 + linear(f, w["w2"], w["b2"])
+    g = {}
+    dy2, g["ln2_g"], g["ln2_b"] = layer_norm_bwd(y2, w["ln2_g"], dout)
+    df, g["w2"], g["b2"] = _linear_bwd(f, w["w2"], dy2)
+    dz = df * gelu_grad(z)
+    dh1_f, g["w1"], g["b1"] = _linear_bwd(h1, w["w1"], dz)
+    dh1 = dy2 + dh1_f
+    dy1, g["ln1_g"], g["ln1_b"] = layer_norm_bwd(y1, w["ln1_g"], dh1)
+    da, g["wo"], g["bo"] = _linear_bwd(a, w["wo"], dy1)
+    dq, dk, dv = attention_bwd(q, k, v, da.reshape(B, L, n_heads, d // n_heads), causal)
+    dx = dy1.copy()
+    for t, wn, bn in ((dq, "wq", "bq"), (dk, "wk", "bk"), (dv, "wv", "bv")):
+        dxi, g[wn], g[bn] = _linear_bwd(x, w[wn], t.reshape(B, L, d))
+        dx += dxi
+    g["x"] = dx
+    return g

@@ -135,3 +135,46 @@ def test_planted_mistakes_fail_the_library_pin(monkeypatch):
             mp.setattr(obpt, attr, fake)
             got = obpt.bpt_layer_fwd(x, w, 2, True)
         assert np.max(np.abs(got - want)) > 1e-6, attr
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_layer_backward_matches_torch_autograd(causal):
+    B, L, d, H, d_ff = 2, 48, 32, 2, 64
+    w = _weights(d, d_ff, seed=11)
+    x = np.random.default_rng(12).standard_normal((B, L, d))
+    dout = np.random.default_rng(13).standard_normal((B, L, d))
+    got = oracle.bpt_layer_bwd(x, w, H, causal, dout)
+    # the same layer from torch's library modules, gradients by autograd
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).requires_grad_(True)   # noqa: E731
+    wt = {k: T(v) for k, v in w.items()}
+    xt = T(x)
+    split = lambda t: t.view(B, L, H, d // H).transpose(1, 2)   # noqa: E731
+    lin = lambda t, n: F.linear(t, wt["w" + n], wt["b" + n])     # noqa: E731
+    a = F.scaled_dot_product_attention(split(lin(xt, "q")), split(lin(xt, "k")),
+                                       split(lin(xt, "v")), is_causal=causal)
+    a = a.transpose(1, 2).reshape(B, L, d)
+    h1 = F.layer_norm(xt + lin(a, "o"), (d,), wt["ln1_g"], wt["ln1_b"], 1e-5)
+    y = F.layer_norm(h1 + lin(F.gelu(lin(h1, "1")), "2"), (d,), wt["ln2_g"], wt["ln2_b"], 1e-5)
+    (y * torch.from_numpy(dout)).sum().backward()
+    assert np.max(np.abs(got["x"] - xt.grad.numpy())) < 1e-10
+    for name in obpt.WEIGHT_NAMES:
+        ref = wt[name].grad.numpy()
+        assert np.max(np.abs(got[name] - ref)) < 1e-10 * max(1.0, np.max(np.abs(ref))), name
+
+
+def test_gelu_and_layer_norm_grads_by_finite_differences():
+    rng = np.random.default_rng(14)
+    z = rng.standard_normal(9) * 2
+    h = 1e-6
+    fd = (oracle.gelu(z + h) - oracle.gelu(z - h)) / (2 * h)
+    assert np.max(np.abs(fd - oracle.gelu_grad(z))) < 1e-8
+    y = rng.standard_normal((3, 16))
+    g, b = 1 + 0.1 * rng.standard_normal(16), rng.standard_normal(16)
+    dout = rng.standard_normal((3, 16))
+    dy, dg, db = oracle.layer_norm_bwd(y, g, dout)
+    f = lambda yy: float(np.sum(oracle.layer_norm(yy, g, b) * dout))   # noqa: E731
+    for (r, c) in [(0, 0), (1, 7), (2, 15)]:
+        yp, ym = y.copy(), y.copy()
+        yp[r, c] += h
+        ym[r, c] -= h
+        assert abs((f(yp) - f(ym)) / (2 * h) - dy[r, c]) < 1e-7
