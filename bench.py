@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-merge", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="layer workload only: forward + backward of the layer per step")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     return a
@@ -480,19 +482,27 @@ def run_ours(args, w, rank, world, local):
 
 # ---------------------------------------------------------------- BPT layer --------
 BPT_METRIC = "blockwise transformer layer forward TFLOP/s (projections, causal ring attention, FFN)"
+BPT_TRAIN_METRIC = "blockwise transformer layer forward + backward TFLOP/s (useful FLOPs)"
 
 
-def bpt_flops(w):
+def bpt_flops(w, train=False):
     """Useful FLOPs of one layer forward: Q, K, V, O projections 4 * 2 L d^2, feed-forward
-    2 * 2 L d d_ff, causal attention 4 D per unmasked pair per head."""
+    2 * 2 L d d_ff, causal attention 4 D per unmasked pair per head.  With the backward:
+    twice the dense forward again (input and weight gradients) and 10 D per pair for the
+    attention (its recompute included); the dense recompute of the BPT backward is not
+    counted."""
     rows = w["batch"] * w["seq_len"]
     d = w["heads"] * w["head_dim"]
-    attn = 4 * w["head_dim"] * w["batch"] * w["heads"] * pairs_of(w["seq_len"], w["causal"])
-    return 8 * rows * d * d + 4 * rows * d * w["d_ff"] + attn
+    pairs = w["batch"] * w["heads"] * pairs_of(w["seq_len"], w["causal"])
+    dense = 8 * rows * d * d + 4 * rows * d * w["d_ff"]
+    if train:
+        return 3 * dense + 14 * w["head_dim"] * pairs
+    return dense + 4 * w["head_dim"] * pairs
 
 
-def bpt_oracle_sample(w, tokens=1024, d=1024, d_ff=4096):
-    """fp64 oracle layer forward on a bounded sample: 1 x `tokens` x d, d_ff, 4 heads."""
+def bpt_oracle_sample(w, tokens=1024, d=1024, d_ff=4096, train=False):
+    """fp64 oracle layer forward (and backward) on a bounded sample: 1 x `tokens` x d,
+    d_ff, d / 128 heads."""
     import numpy as np
     import oracle
     from exact_blockwise_ring_gb300.synthetic import make_bpt_weights, to_f64
@@ -501,9 +511,11 @@ def bpt_oracle_sample(w, tokens=1024, d=1024, d_ff=4096):
     wt = {k: to_f64(v)[0] for k, v in make_bpt_weights(d, d_ff, w["seed"]).items()}
     t0 = time.perf_counter()
     oracle.bpt_layer_fwd(x, wt, d // 128, w["causal"])
+    if train:
+        oracle.bpt_layer_bwd(x, wt, d // 128, w["causal"], rng.standard_normal(x.shape))
     t = time.perf_counter() - t0
     sw = dict(w, batch=1, seq_len=tokens, heads=d // 128, head_dim=128, d_ff=d_ff)
-    return t, bpt_flops(sw) / 1e12, len(os.sched_getaffinity(0))
+    return t, bpt_flops(sw, train) / 1e12, len(os.sched_getaffinity(0))
 
 
 def run_bpt(args, w, rank, world, local):
@@ -522,10 +534,15 @@ def run_bpt(args, w, rank, world, local):
     out = torch.empty((B, L, d), dtype=torch.bfloat16, device=dev)
     ws = era.Workspace(dev)
     stream = torch.cuda.current_stream(dev)
+    train = args.train
+    dout = make_inputs(B, L, 1, d, w["seed"] + 2, device=dev, with_dout=False)[0].view(B, L, d)
 
     def step():
         era.ra_bpt_fwd(x, wt, H, P, blk, w["layout"], w["causal"], block_rows=br, workspace=ws,
-                       out=out)
+                       out=out, train=train)
+        if train:
+            era.ra_bpt_bwd(x, wt, dout, H, P, blk, w["layout"], w["causal"], block_rows=br,
+                           workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -547,7 +564,7 @@ def run_bpt(args, w, rank, world, local):
     clk = clocks.stop()
     ws.check()
     total_ms = dist_max(t0.elapsed_time(t1), world)
-    flops = bpt_flops(w)
+    flops = bpt_flops(w, train)
     value = job_rate(world, flops, K, total_ms)
 
     # dominant kernel: the feed-forward GEMM of one block (rows br, d -> d_ff, GELU), timed
@@ -599,22 +616,27 @@ def run_bpt(args, w, rank, world, local):
                "ms_per_step": round(e_ms / K, 3)}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        t, tf, cores = bpt_oracle_sample(w)
+        t, tf, cores = bpt_oracle_sample(w, train=train)
         cpu = {"value": tf / t, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": "fp64 oracle layer forward, 1 x 1024 tokens, d 1024, d_ff 4096, 8 heads, "
-                         "causal, %.1f s; useful-FLOP convention of the GPU line" % t}
+               "sample": "fp64 oracle layer %s, 1 x 1024 tokens, d 1024, d_ff 4096, 8 heads, "
+                         "causal, %.1f s; useful-FLOP convention of the GPU line"
+                         % ("forward + backward" if train else "forward", t)}
     n_blocks = -(-(B * L) // br)
     # per step: 3 projection GEMMs, the attention (1 kernel, + merge when split), and per
-    # block 3 GEMMs and 2 LayerNorms
-    launches = 3 + 1 + 5 * n_blocks
+    # block 3 GEMMs and 2 LayerNorms; the backward: per block 9 GEMMs, 1 LayerNorm, 1 GELU,
+    # 2 LayerNorm backward, 3 column sums; then the attention's 3 kernels, 6 GEMMs and 3
+    # column sums for the projections, and the dx conversion
+    launches = 3 + 1 + 5 * n_blocks + ((16 * n_blocks + 13) if train else 0)
     if rank == 0:
-        line = {"metric": BPT_METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+        line = {"metric": BPT_TRAIN_METRIC if train else BPT_METRIC, "value": round(value, 2),
+                "unit": "TFLOP/s",
                 "n_gpus": world, "steps": K, "warmup": args.warmup,
                 "ms_per_step": round(total_ms / K, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
-                "config": {"workload": "%s: one blockwise transformer layer forward, %s layout"
-                           % (w["name"], w["layout"]), "batch": B, "seq_len": L, "d_model": d,
+                "config": {"workload": "%s: one blockwise transformer layer %s, %s layout"
+                           % (w["name"], "forward + backward" if train else "forward",
+                              w["layout"]), "batch": B, "seq_len": L, "d_model": d,
                            "heads": H, "d_ff": d_ff, "P": P, "block": blk, "block_rows": br,
                            "causal": w["causal"], "flops_per_step": flops,
                            "l2": "inputs larger than L2 (x %.0f MiB, weights %.0f MiB)"

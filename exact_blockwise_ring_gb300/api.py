@@ -46,6 +46,11 @@ class BptWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in BPT_WEIGHTS]
 
 
+class BptGrads(ctypes.Structure):
+    """Mirror of ra_bpt_grads_t (device pointers)."""
+    _fields_ = [("dx", ctypes.c_void_p)] + [(n, ctypes.c_void_p) for n in BPT_WEIGHTS]
+
+
 EPILOGUES = {"bias": 0, "bias_gelu": 1, "bias_residual": 2}
 
 
@@ -85,6 +90,9 @@ _SIGS = {
     "ra_bpt_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(BptParams)]),
     "ra_bpt_fwd": (ctypes.c_int, [ctypes.POINTER(BptParams), _P, ctypes.POINTER(BptWeights), _P,
                                   ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "ra_bpt_train_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(BptParams)]),
+    "ra_bpt_bwd": (ctypes.c_int, [ctypes.POINTER(BptParams), _P, ctypes.POINTER(BptWeights), _P,
+                                  ctypes.POINTER(BptGrads), _P, ctypes.c_size_t, _P]),
     "ra_last_error_message": (ctypes.c_char_p, []),
 }
 
@@ -342,10 +350,15 @@ def bpt_workspace_bytes(params):
     return lib().ra_bpt_workspace_bytes(ctypes.byref(params))
 
 
+def bpt_train_workspace_bytes(params):
+    return lib().ra_bpt_train_workspace_bytes(ctypes.byref(params))
+
+
 def ra_bpt_fwd(x, weights, heads, P, block, layout="contiguous", causal=True, block_rows=0,
-               out_dtype=torch.bfloat16, workspace=None, stream=None, out=None):
+               out_dtype=torch.bfloat16, workspace=None, stream=None, out=None, train=False):
     """One blockwise transformer layer forward through ra_bpt_fwd.  x [B, L, d] bf16;
-    weights: dict with the names of BPT_WEIGHTS (weights bf16 [out, in], the rest fp32)."""
+    weights: dict with the names of BPT_WEIGHTS (weights bf16 [out, in], the rest fp32).
+    train=True sizes the workspace for a following ra_bpt_bwd, which reuses it."""
     B, L, d = x.shape
     _want(x, torch.bfloat16, "x")
     d_ff = weights["w1"].shape[0]
@@ -363,10 +376,64 @@ def ra_bpt_fwd(x, weights, heads, P, block, layout="contiguous", causal=True, bl
         out = torch.empty((B, L, d), dtype=out_dtype, device=x.device)
     odt = RA_FP32 if out.dtype == torch.float32 else RA_BF16
     ws = workspace or default_workspace(x.device)
-    buf = ws.get(max(bpt_workspace_bytes(prm), 256))
+    need = bpt_train_workspace_bytes(prm) if train else bpt_workspace_bytes(prm)
+    buf = ws.get(max(need, 256))
     _check(lib().ra_bpt_fwd(ctypes.byref(prm), _ptr(x), ctypes.byref(w), _ptr(out), odt,
                             _ptr(buf), buf.numel(), _stream(stream)))
     return out
+
+
+def ra_bpt_bwd(x, weights, dout, heads, P, block, layout="contiguous", causal=True,
+               block_rows=0, workspace=None, stream=None):
+    """Gradients of the layer through ra_bpt_bwd, after ra_bpt_fwd(..., train=True) with the
+    same workspace.  Returns a dict: "x" (bf16, like x) and every name of BPT_WEIGHTS
+    (fp32, shaped like the parameter)."""
+    B, L, d = x.shape
+    _want(x, torch.bfloat16, "x")
+    _want(dout, torch.bfloat16, "dout", tuple(x.shape), x.device)
+    d_ff = weights["w1"].shape[0]
+    prm = make_bpt_params(B, L, heads, d // heads, d_ff, P, block, layout, causal, block_rows)
+    w = BptWeights(*[weights[n].data_ptr() for n in BPT_WEIGHTS])
+    grads = {"x": torch.empty_like(x)}
+    for n in BPT_WEIGHTS:
+        grads[n] = torch.empty(weights[n].shape, dtype=torch.float32, device=x.device)
+    g = BptGrads(grads["x"].data_ptr(), *[grads[n].data_ptr() for n in BPT_WEIGHTS])
+    ws = workspace or default_workspace(x.device)
+    need = bpt_train_workspace_bytes(prm)
+    if ws.buf.numel() < need:
+        raise ValueError("the workspace does not hold the forward's state: run ra_bpt_fwd "
+                         "with train=True and the same workspace first")
+    _check(lib().ra_bpt_bwd(ctypes.byref(prm), _ptr(x), ctypes.byref(w), _ptr(dout),
+                            ctypes.byref(g), _ptr(ws.buf), ws.buf.numel(), _stream(stream)))
+    return grads
+
+
+class BptLayer(torch.autograd.Function):
+    """autograd wrapper of one blockwise transformer layer: forward = ra_bpt_fwd (train
+    mode, its own workspace kept for the backward), backward = ra_bpt_bwd.  Call as
+    BptLayer.apply(x, (heads, P, block, layout, causal, block_rows), *weights in the order
+    of BPT_WEIGHTS); weight gradients come back in fp32 and are cast to the weights'
+    dtypes."""
+
+    @staticmethod
+    def forward(ctx, x, cfg, *params):
+        heads, P, block, layout, causal, block_rows = cfg
+        weights = dict(zip(BPT_WEIGHTS, params))
+        ws = Workspace(x.device)
+        out = ra_bpt_fwd(x, weights, heads, P, block, layout, causal, block_rows, workspace=ws,
+                         train=True)
+        ctx.save_for_backward(x, *params)
+        ctx.cfg, ctx.ws = cfg, ws
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        x, *params = ctx.saved_tensors
+        heads, P, block, layout, causal, block_rows = ctx.cfg
+        weights = dict(zip(BPT_WEIGHTS, params))
+        g = ra_bpt_bwd(x, weights, dout.contiguous(), heads, P, block, layout, causal,
+                       block_rows, workspace=ctx.ws)
+        return (g["x"], None) + tuple(g[n].to(weights[n].dtype) for n in BPT_WEIGHTS)
 
 
 class RingAttention(torch.autograd.Function):

@@ -72,16 +72,21 @@ ra_status_t run_linear(int64_t rows, int in_f, int out_f, const void* x, const v
   return run_gemm(rows, out_f, in_f, x, 0, weight, 0, bias, residual, epi, out, err, st);
 }
 
-// Workspace layout of ra_bpt_fwd (offsets from the base, each 256-byte aligned).
+// Workspace layout (offsets from the base, each 256-byte aligned).  The forward uses the
+// first part; a backward adds the rest (total_train).  The attention region at offset 0 is
+// sized for the attention's forward and backward, so both see the same error word.
 struct BptWs {
   size_t attn, q, k, v, a, lse, y, h1, f, total;
+  size_t z, y2, dy2, dy2f, dy1, da, dxa, dq, dk, dv, total_train;
   int64_t R;
 };
 
 bool bpt_layout(const ra_bpt_params_t* p, BptWs* w) {
   const ra_params_t* a = &p->attn;
-  const size_t attn = ra_fwd_workspace_bytes(a);
+  size_t attn = ra_fwd_workspace_bytes(a);
   if (attn == 0) return false;
+  const size_t attn_b = ra_bwd_workspace_bytes(a);
+  if (attn_b > attn) attn = attn_b;
   const int64_t rows = (int64_t)a->batch * a->seq_len;
   const int64_t d = (int64_t)a->heads * a->head_dim;
   int64_t R = p->block_rows > 0 ? p->block_rows : (rows < 16384 ? rows : 16384);
@@ -98,7 +103,22 @@ bool bpt_layout(const ra_bpt_params_t* p, BptWs* w) {
   w->h1 = off; off += r256((size_t)R * d * 2);
   w->f = off; off += r256((size_t)R * p->d_ff * 2);
   w->total = off;
+  w->z = off; off += r256((size_t)R * p->d_ff * 2);
+  w->y2 = off; off += r256((size_t)R * d * 4);
+  w->dy2 = off; off += r256((size_t)R * d * 2);
+  w->dy2f = off; off += r256((size_t)R * d * 4);
+  w->dy1 = off; off += r256((size_t)R * d * 2);
+  w->da = off; off += r256((size_t)rows * d * 2);
+  w->dxa = off; off += r256((size_t)rows * d * 4);
+  w->dq = off; off += r256((size_t)rows * d * 2);
+  w->dk = off; off += r256((size_t)rows * d * 2);
+  w->dv = off; off += r256((size_t)rows * d * 2);
+  w->total_train = off;
   return true;
+}
+
+ra_status_t cuda_err(cudaError_t e, const char* what) {
+  return e == cudaSuccess ? RA_OK : bfail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
 ra_status_t check_bpt(const ra_bpt_params_t* p) {
@@ -232,6 +252,132 @@ ra_status_t ra_bpt_fwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
     if (e != cudaSuccess) return bfail(RA_ERR_CUDA, "LayerNorm launch: %s", cudaGetErrorString(e));
   }
   return RA_OK;
+}
+
+size_t ra_bpt_train_workspace_bytes(const ra_bpt_params_t* p) {
+  if (check_bpt(p) != RA_OK) return 0;
+  if (p->attn.head_dim != 128 || (long long)p->attn.heads * p->attn.head_dim > 4096) return 0;
+  BptWs w;
+  return bpt_layout(p, &w) ? w.total_train : 0;
+}
+
+ra_status_t ra_bpt_bwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_weights_t* wt,
+                       const void* dout, const ra_bpt_grads_t* gr, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  ra_status_t s = check_bpt(p);
+  if (s != RA_OK) return s;
+  if (p->attn.head_dim != 128)
+    return bfail(RA_ERR_UNSUPPORTED, "the layer's backward needs head_dim 128");
+  if ((long long)p->attn.heads * p->attn.head_dim > 4096)
+    return bfail(RA_ERR_UNSUPPORTED, "the layer's backward needs d_model <= 4096");
+  if (!x || !wt || !dout || !gr) return bfail(RA_ERR_INVALID_ARG, "null pointer");
+  const void* ptrs[] = {wt->wq, wt->wk, wt->wv, wt->wo, wt->w1, wt->w2, wt->bq, wt->bk,
+                        wt->bv, wt->bo, wt->b1, wt->b2, wt->ln1_g, wt->ln1_b, wt->ln2_g,
+                        wt->ln2_b, x, dout, gr->dx, gr->wq, gr->wk, gr->wv, gr->wo, gr->w1,
+                        gr->w2, gr->bq, gr->bk, gr->bv, gr->bo, gr->b1, gr->b2, gr->ln1_g,
+                        gr->ln1_b, gr->ln2_g, gr->ln2_b};
+  for (const void* q : ptrs) {
+    if (!q) return bfail(RA_ERR_INVALID_ARG, "null weight, gradient or tensor pointer");
+    if (!al16(q)) return bfail(RA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  }
+  BptWs w;
+  if (!bpt_layout(p, &w)) return bfail(RA_ERR_INVALID_ARG, "invalid parameters");
+  if (!workspace || workspace_bytes < w.total_train || !al16(workspace))
+    return bfail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu",
+                 w.total_train, workspace_bytes);
+  const ra_params_t* a = &p->attn;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws);
+  const int64_t rows = (int64_t)a->batch * a->seq_len;
+  const int d = a->heads * a->head_dim;
+  const int d_ff = p->d_ff;
+  const float eps = p->ln_eps > 0.f ? p->ln_eps : 1e-5f;
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  const uint8_t* dob = static_cast<const uint8_t*>(dout);
+  uint8_t *Q = ws + w.q, *K = ws + w.k, *V = ws + w.v, *A = ws + w.a;
+  float* lse = reinterpret_cast<float*>(ws + w.lse);
+  float* Y = reinterpret_cast<float*>(ws + w.y);
+  float* Y2 = reinterpret_cast<float*>(ws + w.y2);
+  float* DY2F = reinterpret_cast<float*>(ws + w.dy2f);
+  float* DXA = reinterpret_cast<float*>(ws + w.dxa);
+  void *H1 = ws + w.h1, *F = ws + w.f, *Z = ws + w.z, *DY2 = ws + w.dy2, *DY1 = ws + w.dy1;
+  uint8_t *DA = ws + w.da, *DQ = ws + w.dq, *DK = ws + w.dk, *DV = ws + w.dv;
+
+  // gradients accumulated over blocks start at zero
+  struct { float* p; size_t n; } acc[] = {
+      {gr->wo, (size_t)d * d}, {gr->w1, (size_t)d_ff * d}, {gr->w2, (size_t)d * d_ff},
+      {gr->bq, (size_t)d}, {gr->bk, (size_t)d}, {gr->bv, (size_t)d}, {gr->bo, (size_t)d},
+      {gr->b1, (size_t)d_ff}, {gr->b2, (size_t)d}, {gr->ln1_g, (size_t)d},
+      {gr->ln1_b, (size_t)d}, {gr->ln2_g, (size_t)d}, {gr->ln2_b, (size_t)d}};
+  for (auto& z : acc)
+    if ((s = cuda_err(cudaMemsetAsync(z.p, 0, z.n * 4, st), "cudaMemsetAsync(gradient)")) != RA_OK)
+      return s;
+
+  for (int64_t r0 = 0; r0 < rows; r0 += w.R) {
+    const int64_t R = (rows - r0) < w.R ? (rows - r0) : w.R;
+    const size_t o16 = (size_t)r0 * d * 2;
+    // recompute the block's forward: y1, h1 = LN1(y1), z, f = GELU(z), y2
+    if ((s = run_linear(R, d, d, A + o16, wt->wo, wt->bo, xb + o16, kEpiBiasResidual, Y, err,
+                        st)) != RA_OK)
+      return s;
+    if ((s = cuda_err(launch_layernorm(Y, wt->ln1_g, wt->ln1_b, eps, R, d, H1, 0, st),
+                      "LayerNorm launch")) != RA_OK)
+      return s;
+    if ((s = run_linear(R, d, d_ff, H1, wt->w1, wt->b1, nullptr, kEpiBias, Z, err, st)) != RA_OK)
+      return s;
+    if ((s = cuda_err(launch_gelu(Z, F, (size_t)R * d_ff, st), "GELU launch")) != RA_OK) return s;
+    if ((s = run_linear(R, d_ff, d, F, wt->w2, wt->b2, H1, kEpiBiasResidual, Y2, err, st)) != RA_OK)
+      return s;
+    // LN2 backward: dy2 (fp32 and bf16), dgamma2, dbeta2
+    if ((s = cuda_err(launch_layernorm_bwd(Y2, wt->ln2_g, dob + o16, 0, eps, R, d, DY2F, DY2,
+                                           gr->ln2_g, gr->ln2_b, st),
+                      "LayerNorm backward launch")) != RA_OK)
+      return s;
+    // W2: dW2 += dy2^T f, db2 += sum dy2, dz = (dy2 W2) * GELU'(z) (over z, in place)
+    if ((s = run_gemm(d, d_ff, (int)R, DY2, 1, F, 1, nullptr, gr->w2, kEpiAddF32, gr->w2, err,
+                      st)) != RA_OK ||
+        (s = cuda_err(launch_colsum(DY2F, 1, R, d, gr->b2, st), "column sum")) != RA_OK ||
+        (s = run_gemm(R, d_ff, d, DY2, 0, wt->w2, 1, nullptr, Z, kEpiGeluGrad, Z, err, st)) != RA_OK)
+      return s;
+    // W1: dW1 += dz^T h1, db1 += sum dz, dh1 = dz W1 + dy2 (into the y2 buffer)
+    if ((s = run_gemm(d_ff, d, (int)R, Z, 1, H1, 1, nullptr, gr->w1, kEpiAddF32, gr->w1, err,
+                      st)) != RA_OK ||
+        (s = cuda_err(launch_colsum(Z, 0, R, d_ff, gr->b1, st), "column sum")) != RA_OK ||
+        (s = run_gemm(R, d, d_ff, Z, 0, wt->w1, 1, nullptr, DY2F, kEpiAddF32, Y2, err, st)) != RA_OK)
+      return s;
+    // LN1 backward: dy1 into the dx accumulator (the residual path) and as bf16
+    float* dxa_blk = DXA + (size_t)r0 * d;
+    if ((s = cuda_err(launch_layernorm_bwd(Y, wt->ln1_g, Y2, 1, eps, R, d, dxa_blk, DY1,
+                                           gr->ln1_g, gr->ln1_b, st),
+                      "LayerNorm backward launch")) != RA_OK)
+      return s;
+    // Wo: dWo += dy1^T a, dbo += sum dy1, da = dy1 Wo
+    if ((s = run_gemm(d, d, (int)R, DY1, 1, A + o16, 1, nullptr, gr->wo, kEpiAddF32, gr->wo, err,
+                      st)) != RA_OK ||
+        (s = cuda_err(launch_colsum(dxa_blk, 1, R, d, gr->bo, st), "column sum")) != RA_OK ||
+        (s = run_gemm(R, d, d, DY1, 0, wt->wo, 1, nullptr, nullptr, kEpiPlainBf16, DA + o16, err,
+                      st)) != RA_OK)
+      return s;
+  }
+  // the attention's backward over the whole sequence (its workspace is the first region)
+  if ((s = ra_bwd(a, Q, K, V, A, RA_BF16, lse, DA, DQ, DK, DV, ws + w.attn, w.q, stream)) !=
+      RA_OK)
+    return s;
+  // projections: dx += dQ Wq + dK Wk + dV Wv; dW = d(Q|K|V)^T x; db = column sums
+  const void* dqkv[3] = {DQ, DK, DV};
+  const void* wqkv[3] = {wt->wq, wt->wk, wt->wv};
+  float* gw[3] = {gr->wq, gr->wk, gr->wv};
+  float* gb[3] = {gr->bq, gr->bk, gr->bv};
+  for (int t = 0; t < 3; ++t) {
+    if ((s = run_gemm(rows, d, d, dqkv[t], 0, wqkv[t], 1, nullptr, DXA, kEpiAddF32, DXA, err,
+                      st)) != RA_OK ||
+        (s = run_gemm(d, d, (int)rows, dqkv[t], 1, x, 1, nullptr, nullptr, kEpiPlainF32, gw[t],
+                      err, st)) != RA_OK ||
+        (s = cuda_err(launch_colsum(dqkv[t], 0, rows, d, gb[t], st), "column sum")) != RA_OK)
+      return s;
+  }
+  return cuda_err(launch_dq_convert(DXA, gr->dx, 1.0f, (size_t)rows * d, st), "dx convert");
 }
 
 }  // extern "C"

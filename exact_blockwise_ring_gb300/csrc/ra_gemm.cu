@@ -361,6 +361,172 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// LayerNorm backward over rows of d features (d % 512 == 0, d <= 4096), kBwdRows rows per
+// CTA of 128 threads, each thread owning d / 128 features:
+//   yh = (y - mean) * rstd,  dyh = dout * gamma,
+//   dy = rstd * (dyh - mean(dyh) - yh * mean(dyh * yh)),
+//   dgamma += sum_rows dout * yh,  dbeta += sum_rows dout  (fp32 atomics once per CTA).
+// y is the LayerNorm's fp32 input; dout bf16 or fp32; dy written as fp32 and/or bf16.
+constexpr int kBwdRows = 16;
+
+template <int DOUT_F32>
+__global__ void __launch_bounds__(128)
+    layernorm_bwd_kernel(const float* __restrict__ y, const float* __restrict__ gamma,
+                         const void* __restrict__ dout, float eps, int d, long long rows,
+                         float* dy_f32, __nv_bfloat16* dy_bf16, float* dgamma, float* dbeta) {
+  constexpr int kMaxV = 8;
+  __shared__ float red[2][4];
+  const int nv = d / 512;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float dg[kMaxV][4], db[kMaxV][4];
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dg[i][c] = db[i][c] = 0.f;
+  const long long r0 = (long long)blockIdx.x * kBwdRows;
+  for (long long row = r0; row < r0 + kBwdRows && row < rows; ++row) {
+    const float4* yr = reinterpret_cast<const float4*>(y + row * d);
+    float yv[kMaxV][4], go[kMaxV][4];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      if (i < nv) {
+        const float4 t = __ldg(yr + i * 128 + threadIdx.x);
+        yv[i][0] = t.x; yv[i][1] = t.y; yv[i][2] = t.z; yv[i][3] = t.w;
+        s += (t.x + t.y) + (t.z + t.w);
+        const size_t e = (size_t)row * d + (size_t)(i * 128 + threadIdx.x) * 4;
+        if (DOUT_F32) {
+          const float4 o = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(dout) + e));
+          go[i][0] = o.x; go[i][1] = o.y; go[i][2] = o.z; go[i][3] = o.w;
+        } else {
+          const uint2 o = __ldg(reinterpret_cast<const uint2*>(
+              static_cast<const __nv_bfloat16*>(dout) + e));
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.y));
+          go[i][0] = a.x; go[i][1] = a.y; go[i][2] = b.x; go[i][3] = b.y;
+        }
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    __syncthreads();                               // red[] reuse across rows
+    if (lane == 0) red[0][w] = s;
+    __syncthreads();
+    const float mean = (red[0][0] + red[0][1] + red[0][2] + red[0][3]) / d;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      if (i < nv)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float t = yv[i][c] - mean;
+          q += t * t;
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    if (lane == 0) red[1][w] = q;
+    __syncthreads();
+    const float rstd = rsqrtf((red[1][0] + red[1][1] + red[1][2] + red[1][3]) / d + eps);
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      if (i < nv) {
+        const int f0 = (i * 128 + threadIdx.x) * 4;
+        const float4 gg = __ldg(reinterpret_cast<const float4*>(gamma + f0));
+        const float gv[4] = {gg.x, gg.y, gg.z, gg.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float yh = (yv[i][c] - mean) * rstd;
+          const float dyh = go[i][c] * gv[c];
+          dg[i][c] += go[i][c] * yh;
+          db[i][c] += go[i][c];
+          yv[i][c] = yh;                          // keep yh, dyh for the last step
+          go[i][c] = dyh;
+          s1 += dyh;
+          s2 += dyh * yh;
+        }
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    __syncthreads();
+    if (lane == 0) {
+      red[0][w] = s1;
+      red[1][w] = s2;
+    }
+    __syncthreads();
+    const float m1 = (red[0][0] + red[0][1] + red[0][2] + red[0][3]) / d;
+    const float m2 = (red[1][0] + red[1][1] + red[1][2] + red[1][3]) / d;
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      if (i < nv) {
+        float o[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[c] = rstd * (go[i][c] - m1 - yv[i][c] * m2);
+        const size_t e = (size_t)row * d + (size_t)(i * 128 + threadIdx.x) * 4;
+        if (dy_f32) *reinterpret_cast<float4*>(dy_f32 + e) = make_float4(o[0], o[1], o[2], o[3]);
+        if (dy_bf16)
+          *reinterpret_cast<uint2*>(dy_bf16 + e) =
+              make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+      }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+    if (i < nv)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int f = (i * 128 + threadIdx.x) * 4 + c;
+        atomicAdd(dgamma + f, dg[i][c]);
+        atomicAdd(dbeta + f, db[i][c]);
+      }
+}
+
+// out[c] += sum over rows of x[row, c], x bf16 or fp32 [rows, n]; each thread sums 4
+// columns over kSumRows rows, then one atomic per column.
+constexpr int kSumRows = 256;
+
+template <int X_F32>
+__global__ void __launch_bounds__(256)
+    colsum_kernel(const void* __restrict__ x, long long rows, int n, float* out) {
+  const int c0 = (blockIdx.x * 256 + threadIdx.x) * 4;
+  if (c0 >= n) return;
+  const long long r0 = (long long)blockIdx.y * kSumRows;
+  const long long r1 = r0 + kSumRows < rows ? r0 + kSumRows : rows;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  for (long long r = r0; r < r1; ++r) {
+    const size_t e = (size_t)r * n + c0;
+    if (X_F32) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + e));
+      a0 += v.x; a1 += v.y; a2 += v.z; a3 += v.w;
+    } else {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(x) + e));
+      const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      a0 += p.x; a1 += p.y; a2 += q.x; a3 += q.y;
+    }
+  }
+  atomicAdd(out + c0, a0);
+  atomicAdd(out + c0 + 1, a1);
+  atomicAdd(out + c0 + 2, a2);
+  atomicAdd(out + c0 + 3, a3);
+}
+
+// f = GELU(z), bf16, 8 elements per thread.
+__global__ void __launch_bounds__(256) gelu_kernel(const __nv_bfloat16* __restrict__ z,
+                                                   __nv_bfloat16* __restrict__ f, size_t n8) {
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n8;
+       v += (size_t)gridDim.x * blockDim.x) {
+    float a[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(z) + v), a);
+    reinterpret_cast<uint4*>(f)[v] =
+        make_uint4(pack_bf16x2(gelu_exact(a[0]), gelu_exact(a[1])),
+                   pack_bf16x2(gelu_exact(a[2]), gelu_exact(a[3])),
+                   pack_bf16x2(gelu_exact(a[4]), gelu_exact(a[5])),
+                   pack_bf16x2(gelu_exact(a[6]), gelu_exact(a[7])));
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -381,7 +547,7 @@ bool gemm_supported(int epi, int a_mn, int b_mn) {
   if (!a_mn && !b_mn) return epi >= kEpiBias && epi <= kEpiPlainBf16;
   if (!a_mn && b_mn)
     return epi == kEpiPlainF32 || epi == kEpiGeluGrad || epi == kEpiAddF32 || epi == kEpiPlainBf16;
-  if (a_mn && b_mn) return epi == kEpiPlainF32;
+  if (a_mn && b_mn) return epi == kEpiPlainF32 || epi == kEpiAddF32;
   return false;
 }
 
@@ -415,6 +581,7 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensor
       default: return launch_one<kEpiPlainBf16, 0, 1>(g, ta, tb, grid, s);
     }
   }
+  if (epi == kEpiAddF32) return launch_one<kEpiAddF32, 1, 1>(g, ta, tb, grid, s);
   return launch_one<kEpiPlainF32, 1, 1>(g, ta, tb, grid, s);
 }
 
@@ -425,6 +592,44 @@ cudaError_t launch_layernorm(const float* x, const float* gamma, const float* be
     layernorm_kernel<1><<<(unsigned)rows, 128, 0, s>>>(x, gamma, beta, eps, d, out);
   else
     layernorm_kernel<0><<<(unsigned)rows, 128, 0, s>>>(x, gamma, beta, eps, d, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm_bwd(const float* y, const float* gamma, const void* dout,
+                                 int dout_f32, float eps, long long rows, int d, float* dy_f32,
+                                 void* dy_bf16, float* dgamma, float* dbeta, cudaStream_t s) {
+  if (d % 512 != 0 || d > 4096 || rows <= 0) return cudaErrorInvalidValue;
+  const long long grid = (rows + kBwdRows - 1) / kBwdRows;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(dy_bf16);
+  if (dout_f32)
+    layernorm_bwd_kernel<1><<<(unsigned)grid, 128, 0, s>>>(y, gamma, dout, eps, d, rows, dy_f32,
+                                                            o16, dgamma, dbeta);
+  else
+    layernorm_bwd_kernel<0><<<(unsigned)grid, 128, 0, s>>>(y, gamma, dout, eps, d, rows, dy_f32,
+                                                            o16, dgamma, dbeta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsum(const void* x, int x_f32, long long rows, int n, float* out,
+                          cudaStream_t s) {
+  if (n % 4 != 0 || rows <= 0) return cudaErrorInvalidValue;
+  const long long gy = (rows + kSumRows - 1) / kSumRows;
+  if (gy > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((n / 4 + 255) / 256), (unsigned)gy);
+  if (x_f32) colsum_kernel<1><<<grid, 256, 0, s>>>(x, rows, n, out);
+  else colsum_kernel<0><<<grid, 256, 0, s>>>(x, rows, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gelu(const void* z, void* f, size_t n, cudaStream_t s) {
+  if (n % 8 != 0) return cudaErrorInvalidValue;
+  const size_t n8 = n / 8;
+  long long blocks = (long long)((n8 + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  gelu_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(z),
+                                              static_cast<__nv_bfloat16*>(f), n8);
   return cudaGetLastError();
 }
 

@@ -195,6 +195,12 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensor
                         int a_mn, int b_mn, cudaStream_t s);
 cudaError_t launch_layernorm(const float* x, const float* gamma, const float* beta, float eps,
                              long long rows, int d, void* out, int out_fp32, cudaStream_t s);
+cudaError_t launch_layernorm_bwd(const float* y, const float* gamma, const void* dout,
+                                 int dout_f32, float eps, long long rows, int d, float* dy_f32,
+                                 void* dy_bf16, float* dgamma, float* dbeta, cudaStream_t s);
+cudaError_t launch_colsum(const void* x, int x_f32, long long rows, int n, float* out,
+                          cudaStream_t s);
+cudaError_t launch_gelu(const void* z, void* f, size_t n, cudaStream_t s);
 
 // Launchers (defined next to their kernels).
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -309,15 +309,55 @@ typedef struct {
 } ra_bpt_weights_t;
 
 /* Bytes of workspace ra_bpt_fwd needs (0 if `p` is invalid): the attention's workspace
- * (whose error word is the layer's), Q, K, V and the attention output (bf16 [B*L, d]
- * each), lse, and one block's fp32 [block_rows, d] and bf16 [block_rows, d] and
- * [block_rows, d_ff] buffers.  Zero-filled before first use. */
+ * (sized for its forward and backward; its error word is the layer's), Q, K, V and the
+ * attention output (bf16 [B*L, d] each), lse, and one block's fp32 [block_rows, d] and
+ * bf16 [block_rows, d] and [block_rows, d_ff] buffers.  Zero-filled before first use. */
 size_t ra_bpt_workspace_bytes(const ra_bpt_params_t* p);
 
 /* x [batch, seq_len, d] bf16 (tokens in natural order), out same shape of out_dtype. */
 ra_status_t ra_bpt_fwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_weights_t* w,
                        void* out, int out_dtype, void* workspace, size_t workspace_bytes,
                        void* stream);
+
+/* Gradients of the layer, all device pointers: dx bf16 [batch, seq_len, d]; the others
+ * fp32, shaped like the parameter of the same name.  ra_bpt_bwd overwrites every one. */
+typedef struct {
+  void* dx;
+  float* wq;
+  float* wk;
+  float* wv;
+  float* wo;
+  float* w1;
+  float* w2;
+  float* bq;
+  float* bk;
+  float* bv;
+  float* bo;
+  float* b1;
+  float* b2;
+  float* ln1_g;
+  float* ln1_b;
+  float* ln2_g;
+  float* ln2_b;
+} ra_bpt_grads_t;
+
+/* Bytes of workspace for a forward followed by a backward (>= ra_bpt_workspace_bytes; the
+ * forward's part of the layout is the same), 0 if `p` is invalid or has no backward
+ * kernel (head_dim must be 128 and d_model <= 4096). */
+size_t ra_bpt_train_workspace_bytes(const ra_bpt_params_t* p);
+
+/*
+ * Backward of the layer: given dout (bf16 [batch, seq_len, d]) = d loss / d out, writes
+ * every gradient of `g`.  Must follow ra_bpt_fwd on the same x, weights and workspace
+ * (whose Q, K, V, attention output and lse it reuses); the workspace must hold
+ * ra_bpt_train_workspace_bytes.  Per block of rows it recomputes the forward's Wo,
+ * LayerNorm, W1 and W2 steps (memory stays per block), then runs the LayerNorm, GELU and
+ * Linear backward steps (weight gradients accumulated in fp32 across blocks), and finally
+ * the attention backward (ra_bwd) over the whole sequence and the projections' backward.
+ */
+ra_status_t ra_bpt_bwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_weights_t* w,
+                       const void* dout, const ra_bpt_grads_t* g, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

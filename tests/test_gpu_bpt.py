@@ -134,3 +134,61 @@ def test_bpt_fullsize_sampled_rows():
     err = got - ref
     assert np.linalg.norm(err) / np.linalg.norm(ref) <= 1e-2
     assert np.all(np.abs(err) <= 5e-2 + 2.0 ** -8 * np.abs(ref))
+
+
+def _layer_grads_case(B, L, H, d_ff, seed):
+    d = H * 128
+    x = make_inputs(B, L, 1, d, seed, with_dout=False)[0].view(B, L, d)
+    dout = make_inputs(B, L, 1, d, seed + 1, with_dout=False)[0].view(B, L, d)
+    w = make_bpt_weights(d, d_ff, seed + 2)
+    ref = oracle.bpt_layer_bwd(_f64(x), {k: _f64(v) for k, v in w.items()}, H, True, _f64(dout))
+    return x, dout, w, ref
+
+
+@pytest.mark.parametrize("layout,B,block_rows", [("striped", 1, 256), ("zigzag", 2, 384),
+                                                 ("contiguous", 1, 0)])
+def test_bpt_backward_parity(layout, B, block_rows):
+    """Every gradient within 2e-2 relative Frobenius error of the fp64 chain rule (as for the
+    attention's gradients).  The K bias's gradient is exactly zero (adding a vector to every
+    key shifts each query's scores by a constant), so it is checked as that identity."""
+    H, d_ff, P, L = 4, 1024, 4, 1024
+    x, dout, w, ref = _layer_grads_case(B, L, H, d_ff, seed=80)
+    wd = {k: v.cuda() for k, v in w.items()}
+    ws = era.Workspace("cuda")
+    era.ra_bpt_fwd(x.cuda(), wd, H, P, 128, layout, True, block_rows=block_rows, workspace=ws,
+                   train=True)
+    g = era.ra_bpt_bwd(x.cuda(), wd, dout.cuda(), H, P, 128, layout, True, block_rows=block_rows,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    ws.check()
+    errs = {}
+    for n in ["x"] + [n for n in era.BPT_WEIGHTS if n != "bk"]:
+        errs[n] = float(np.linalg.norm(_f64(g[n]) - ref[n]) / np.linalg.norm(ref[n]))
+    assert max(errs.values()) <= 2e-2, errs
+    assert float(np.linalg.norm(_f64(g["bk"]))) <= 2e-2 * float(np.linalg.norm(ref["bv"]))
+
+
+def test_bpt_autograd_and_blocking():
+    """BptLayer through torch autograd gives ra_bpt_bwd's gradients; a different block size
+    changes only the fp32 summation order of the weight gradients."""
+    H, d_ff, P, L = 4, 512, 4, 1024
+    x, dout, w, _ = _layer_grads_case(1, L, H, d_ff, seed=90)
+    xd = x.cuda().requires_grad_(True)
+    params = [w[n].cuda().requires_grad_(True) for n in era.BPT_WEIGHTS]
+    out = era.BptLayer.apply(xd, (H, P, 128, "zigzag", True, 256), *params)
+    out.backward(dout.cuda())
+    wd = {n: p.detach() for n, p in zip(era.BPT_WEIGHTS, params)}
+    ws = era.Workspace("cuda")
+    out2 = era.ra_bpt_fwd(x.cuda(), wd, H, P, 128, "zigzag", True, block_rows=512, workspace=ws,
+                          train=True)
+    g = era.ra_bpt_bwd(x.cuda(), wd, dout.cuda(), H, P, 128, "zigzag", True, block_rows=512,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.detach(), out2)
+    assert float((xd.grad.float() - g["x"].float()).abs().max()) <= 1e-2
+    for n, p in zip(era.BPT_WEIGHTS, params):
+        if n == "bk":                       # exactly zero in exact arithmetic: noise only
+            continue
+        ref = g[n].to(p.dtype).float()
+        den = float(ref.norm()) or 1.0
+        assert float((p.grad.float() - ref).norm()) <= 1e-2 * den + 1e-6, n
