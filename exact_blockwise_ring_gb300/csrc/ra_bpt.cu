@@ -42,7 +42,7 @@ ra_status_t check_linear(int64_t rows, int in_f, int out_f, int epi) {
 // [N, K] (b_mn = 0) or [K, N] (b_mn = 1); shapes already checked.
 ra_status_t run_gemm(int64_t M, int N, int K, const void* a, int a_mn, const void* b, int b_mn,
                      const float* bias, const void* aux, int epi, void* out, unsigned int* err,
-                     cudaStream_t st) {
+                     cudaStream_t st, void* out2 = nullptr) {
   CUtensorMap ta, tb;
   ra_status_t s;
   if (a_mn) s = encode_2d_bf16(&ta, a, M, K, 64, 64);
@@ -58,6 +58,7 @@ ra_status_t run_gemm(int64_t M, int N, int K, const void* a, int a_mn, const voi
   g.bias = bias;
   g.aux = aux;
   g.out = out;
+  g.out2 = out2;
   g.err = err;
   g.wait_limit_ns = kWaitLimitNs;
   cudaError_t e = launch_gemm(g, ta, tb, epi, a_mn, b_mn, st);
@@ -324,9 +325,10 @@ ra_status_t ra_bpt_bwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
     if ((s = cuda_err(launch_layernorm(Y, wt->ln1_g, wt->ln1_b, eps, R, d, H1, 0, st),
                       "LayerNorm launch")) != RA_OK)
       return s;
-    if ((s = run_linear(R, d, d_ff, H1, wt->w1, wt->b1, nullptr, kEpiBias, Z, err, st)) != RA_OK)
+    // f = GELU(z) exactly as the forward rounded it, and z itself for GELU'
+    if ((s = run_gemm(R, d_ff, d, H1, 0, wt->w1, 0, wt->b1, nullptr, kEpiBiasGeluZ, F, err, st,
+                      Z)) != RA_OK)
       return s;
-    if ((s = cuda_err(launch_gelu(Z, F, (size_t)R * d_ff, st), "GELU launch")) != RA_OK) return s;
     if ((s = run_linear(R, d_ff, d, F, wt->w2, wt->b2, H1, kEpiBiasResidual, Y2, err, st)) != RA_OK)
       return s;
     // LN2 backward: dy2 (fp32 and bf16), dgamma2, dbeta2

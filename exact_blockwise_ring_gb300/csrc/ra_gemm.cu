@@ -240,7 +240,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float f[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);
-        if (EPI == kEpiBias || EPI == kEpiBiasGelu || EPI == kEpiBiasResidual) {
+        if (EPI == kEpiBias || EPI == kEpiBiasGelu || EPI == kEpiBiasResidual ||
+            EPI == kEpiBiasGeluZ) {
           const float4* bias4 = reinterpret_cast<const float4*>(g.bias + col);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -251,7 +252,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             f[4 * e + 3] += bb.w;
           }
         }
-        if (EPI == kEpiBiasGelu) {
+        if (EPI == kEpiBiasGeluZ) {                // the pre-activation, as bf16
+          uint4* o2 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(g.out2) + e0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            o2[e] = make_uint4(pack_bf16x2(f[8 * e], f[8 * e + 1]), pack_bf16x2(f[8 * e + 2], f[8 * e + 3]),
+                               pack_bf16x2(f[8 * e + 4], f[8 * e + 5]),
+                               pack_bf16x2(f[8 * e + 6], f[8 * e + 7]));
+        }
+        if (EPI == kEpiBiasGelu || EPI == kEpiBiasGeluZ) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) f[e] = gelu_exact(f[e]);
         }
@@ -512,21 +521,6 @@ __global__ void __launch_bounds__(256)
   atomicAdd(out + c0 + 3, a3);
 }
 
-// f = GELU(z), bf16, 8 elements per thread.
-__global__ void __launch_bounds__(256) gelu_kernel(const __nv_bfloat16* __restrict__ z,
-                                                   __nv_bfloat16* __restrict__ f, size_t n8) {
-  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n8;
-       v += (size_t)gridDim.x * blockDim.x) {
-    float a[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(z) + v), a);
-    reinterpret_cast<uint4*>(f)[v] =
-        make_uint4(pack_bf16x2(gelu_exact(a[0]), gelu_exact(a[1])),
-                   pack_bf16x2(gelu_exact(a[2]), gelu_exact(a[3])),
-                   pack_bf16x2(gelu_exact(a[4]), gelu_exact(a[5])),
-                   pack_bf16x2(gelu_exact(a[6]), gelu_exact(a[7])));
-  }
-}
-
 }  // namespace
 
 namespace {
@@ -544,7 +538,7 @@ cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& ta, const CUtensorM
 }  // namespace
 
 bool gemm_supported(int epi, int a_mn, int b_mn) {
-  if (!a_mn && !b_mn) return epi >= kEpiBias && epi <= kEpiPlainBf16;
+  if (!a_mn && !b_mn) return epi >= kEpiBias && epi <= kEpiBiasGeluZ;
   if (!a_mn && b_mn)
     return epi == kEpiPlainF32 || epi == kEpiGeluGrad || epi == kEpiAddF32 || epi == kEpiPlainBf16;
   if (a_mn && b_mn) return epi == kEpiPlainF32 || epi == kEpiAddF32;
@@ -570,6 +564,7 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensor
       case kEpiPlainF32: return launch_one<kEpiPlainF32, 0, 0>(g, ta, tb, grid, s);
       case kEpiGeluGrad: return launch_one<kEpiGeluGrad, 0, 0>(g, ta, tb, grid, s);
       case kEpiAddF32: return launch_one<kEpiAddF32, 0, 0>(g, ta, tb, grid, s);
+      case kEpiBiasGeluZ: return launch_one<kEpiBiasGeluZ, 0, 0>(g, ta, tb, grid, s);
       default: return launch_one<kEpiPlainBf16, 0, 0>(g, ta, tb, grid, s);
     }
   }
@@ -619,17 +614,6 @@ cudaError_t launch_colsum(const void* x, int x_f32, long long rows, int n, float
   const dim3 grid((unsigned)((n / 4 + 255) / 256), (unsigned)gy);
   if (x_f32) colsum_kernel<1><<<grid, 256, 0, s>>>(x, rows, n, out);
   else colsum_kernel<0><<<grid, 256, 0, s>>>(x, rows, n, out);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gelu(const void* z, void* f, size_t n, cudaStream_t s) {
-  if (n % 8 != 0) return cudaErrorInvalidValue;
-  const size_t n8 = n / 8;
-  long long blocks = (long long)((n8 + 255) / 256);
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (blocks < 1) blocks = 1;
-  gelu_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(z),
-                                              static_cast<__nv_bfloat16*>(f), n8);
   return cudaGetLastError();
 }
 

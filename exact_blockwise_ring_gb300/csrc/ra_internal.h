@@ -172,9 +172,11 @@ struct BwdArgs {
 //   kEpiGeluGrad      bf16  acc * GELU'(aux), aux = the GELU's input z (bf16 [M, N])
 //   kEpiAddF32        fp32  acc + aux (fp32 [M, N])
 //   kEpiPlainBf16     bf16  acc
+//   kEpiBiasGeluZ     bf16  GELU(acc + bias), and bf16 acc + bias into out2 (the same fp32
+//                     value rounded before and after GELU, as the forward rounds it)
 enum GemmEpilogue : int {
   kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResidual = 2, kEpiPlainF32 = 3, kEpiGeluGrad = 4,
-  kEpiAddF32 = 5, kEpiPlainBf16 = 6
+  kEpiAddF32 = 5, kEpiPlainBf16 = 6, kEpiBiasGeluZ = 7
 };
 
 // out[M, N] = epilogue(sum_k A[m, k] B[n, k]); M % 128, N % 256, K % 64 == 0.  A is read
@@ -183,9 +185,10 @@ enum GemmEpilogue : int {
 // kEpiGeluGrad, kEpiAddF32, kEpiPlainBf16, and (1, 1) with kEpiPlainF32.
 struct GemmArgs {
   int M, N, K;
-  const float* bias;        // [N] fp32 (kEpiBias, kEpiBiasGelu, kEpiBiasResidual)
+  const float* bias;        // [N] fp32 (kEpiBias*, the GELU ones, kEpiBiasResidual)
   const void* aux;          // [M, N] operand of kEpiBiasResidual, kEpiGeluGrad, kEpiAddF32
   void* out;
+  void* out2;               // [M, N] second output of kEpiBiasGeluZ
   unsigned int* err;        // workspace error word
   uint64_t wait_limit_ns;
 };
@@ -200,7 +203,7 @@ cudaError_t launch_layernorm_bwd(const float* y, const float* gamma, const void*
                                  void* dy_bf16, float* dgamma, float* dbeta, cudaStream_t s);
 cudaError_t launch_colsum(const void* x, int x_f32, long long rows, int n, float* out,
                           cudaStream_t s);
-cudaError_t launch_gelu(const void* z, void* f, size_t n, cudaStream_t s);
+
 
 // Launchers (defined next to their kernels).
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,

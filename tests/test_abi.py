@@ -212,3 +212,22 @@ def test_layer_bindings_check_their_inputs_before_any_call():
         era.ra_layernorm(torch.zeros((4, 512)), torch.ones(512), torch.zeros(512))
     with pytest.raises(ValueError, match="CUDA"):
         era.ra_bpt_fwd(torch.zeros((1, 1024, 512), dtype=torch.bfloat16), {}, 4, 4, 128)
+
+
+def test_bpt_train_workspace_and_backward_checks(L):
+    prm = era.make_bpt_params(1, 1024, 4, 128, 1024, 4, 128, "striped", True, 256)
+    assert era.bpt_train_workspace_bytes(prm) > era.bpt_workspace_bytes(prm) > 0
+    # head_dim 64 has a forward but no backward kernel; d_model 8192 > 4096 likewise
+    p64 = era.make_bpt_params(1, 1024, 8, 64, 1024, 4, 128, "striped", True, 256)
+    assert era.bpt_workspace_bytes(p64) > 0 and era.bpt_train_workspace_bytes(p64) == 0
+    big = era.make_bpt_params(1, 1024, 64, 128, 1024, 4, 128, "striped", True, 256)
+    assert era.bpt_workspace_bytes(big) > 0 and era.bpt_train_workspace_bytes(big) == 0
+    w = api.BptWeights(*([FAKE.value] * len(api.BPT_WEIGHTS)))
+    gr = api.BptGrads(*([FAKE.value] * (1 + len(api.BPT_WEIGHTS))))
+    assert L.ra_bpt_bwd(ctypes.byref(p64), FAKE, ctypes.byref(w), FAKE, ctypes.byref(gr), FAKE,
+                        1 << 40, None) == 2
+    gr_null = api.BptGrads(*([None] + [FAKE.value] * len(api.BPT_WEIGHTS)))
+    assert L.ra_bpt_bwd(ctypes.byref(prm), FAKE, ctypes.byref(w), FAKE, ctypes.byref(gr_null),
+                        FAKE, 1 << 40, None) == 1
+    assert L.ra_bpt_bwd(ctypes.byref(prm), FAKE, ctypes.byref(w), FAKE, ctypes.byref(gr), FAKE,
+                        64, None) == 3

@@ -192,3 +192,35 @@ def test_bpt_autograd_and_blocking():
         ref = g[n].to(p.dtype).float()
         den = float(ref.norm()) or 1.0
         assert float((p.grad.float() - ref).norm()) <= 1e-2 * den + 1e-6, n
+
+
+def test_bpt_backward_fullsize_identities():
+    """The 32k layer workload's forward + backward in the configuration bench.py times,
+    checked through identities that hold at any size: d ln2_b = sum over rows of dout;
+    d ln2_g = sum over rows of dout * (out - ln2_b) / ln2_g (the normalised value, read
+    back from the fp32 forward output); the K bias's gradient vanishes."""
+    from exact_blockwise_ring_gb300.synthetic import WORKLOADS, SEEDS
+    wl = WORKLOADS["32k-bpt"]
+    B, L, H, D, P, blk = (wl["batch"], wl["seq_len"], wl["heads"], wl["head_dim"], wl["P"],
+                          wl["block"])
+    d, d_ff, br = H * D, wl["d_ff"], wl["block_rows"]
+    dev = torch.device("cuda:0")
+    x = make_inputs(B, L, 1, d, SEEDS["32k-bpt"], device=dev, with_dout=False)[0].view(B, L, d)
+    dout = make_inputs(B, L, 1, d, SEEDS["32k-bpt"] + 2, device=dev,
+                       with_dout=False)[0].view(B, L, d)
+    w = make_bpt_weights(d, d_ff, SEEDS["32k-bpt"] + 1, device=dev)
+    ws = era.Workspace(dev)
+    out = era.ra_bpt_fwd(x, w, H, P, blk, "zigzag", True, block_rows=br, workspace=ws,
+                         out_dtype=torch.float32, train=True)
+    g = era.ra_bpt_bwd(x, w, dout, H, P, blk, "zigzag", True, block_rows=br, workspace=ws)
+    torch.cuda.synchronize()
+    ws.check()
+    do64 = dout.double().view(-1, d)
+    want_b = do64.sum(0)
+    assert float((g["ln2_b"].double() - want_b).norm() / want_b.norm()) <= 1e-4
+    yhat = (out.double().view(-1, d) - w["ln2_b"].double()) / w["ln2_g"].double()
+    want_g = (do64 * yhat).sum(0)
+    assert float((g["ln2_g"].double() - want_g).norm() / want_g.norm()) <= 1e-3
+    assert float(g["bk"].norm()) <= 2e-2 * float(g["bv"].norm())
+    for n, t in g.items():
+        assert torch.isfinite(t).all(), n
