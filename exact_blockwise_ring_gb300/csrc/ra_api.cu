@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "ra_internal.h"
+#include "ra_layer.h"
 
 namespace ra {
 namespace {

@@ -5,6 +5,7 @@
 #include <cstdio>
 
 #include "ra_internal.h"
+#include "ra_layer.h"
 
 namespace ra {
 namespace {

@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 
 #include "ra_internal.h"
+#include "ra_layer.h"
 #include "ra_ptx.cuh"
 
 namespace ra {
