@@ -53,6 +53,9 @@ def _fwd(L, prm, q=FAKE, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30, odt=0, s
 @pytest.mark.parametrize("kw,code", [
     (dict(seq_len=1000), 1),              # not divisible by P * block
     (dict(batch=0), 1),
+    (dict(seq_len=0), 1),                 # empty sequence
+    (dict(seq_len=-1024), 1),
+    (dict(seq_len=1 << 33, heads=1024, P=8), 1),   # past the 2^40-element guard
     (dict(heads=0), 1),
     (dict(P=0), 1),
     (dict(P=2000, seq_len=2000 * 128), 1),
