@@ -460,6 +460,22 @@ def run_ours(args, w, rank, world, local):
             "frac_bwd": round(pairs / (main_ms * 1e-3) / ceil, 4),
             "ceiling_kind": "31 exp2/clk/SM (microbenchmark on this part) x 152 SMs x median SM clock"}
 
+    # per-shard causal work: the host model for every layout (equal to the device counters,
+    # which the tests check bit for bit) and the device counters of this layout, from one
+    # forward outside the timed region
+    balance = {}
+    for lay in ("contiguous", "striped", "zigzag"):
+        try:
+            m = era.ra_shard_work_model(L, P, blk, lay, causal)
+        except Exception:            # e.g. zigzag needs L divisible by 2 * P * block
+            continue
+        balance[lay] = {u: round(max(m[u]) / (sum(m[u]) / P), 5) for u in ("tiles", "pairs", "visits")}
+    _, _, sw = era.ra_fwd(q, k, v, P, blk, layout, causal, shard_work=True, workspace=ws)
+    swc = sw.cpu().double()
+    balance["device_" + layout] = {u: round(float(swc[n].max() / swc[n].mean()), 5)
+                                   for n, u in enumerate(("tiles", "pairs", "visits"))}
+    balance["unit"] = "max / mean over the P shards"
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
@@ -473,7 +489,8 @@ def run_ours(args, w, rank, world, local):
                 "config": config_of(w),
                 "stage_ms": {"fwd": round(fwd_ms, 3), "bwd_preprocess": round(pre_ms, 3),
                              "bwd_main": round(main_ms, 3), "bwd_finalize": round(fin_ms, 3)},
-                "roofline": roofline, "hbm_kernels": hbm_kernels, "cpu_baseline": cpu,
+                "roofline": roofline, "hbm_kernels": hbm_kernels, "shard_balance": balance,
+                "cpu_baseline": cpu,
                 "e2e": e2e,
                 "tflops_12d": round(value * 12.0 / 14.0, 2),
                 "mufu": mufu, "gpu_launches": 4 * K, "clocks": clk}
