@@ -21,7 +21,8 @@ post-norm transformer layer.  Written out, for x [B, L, d]:
     GELU(z) = z * Phi(z) = z / 2 * (1 + erf(z / sqrt(2)))   (the exact form).
 
 The page's layer shows no mask; the attention here takes the same `causal` switch as the
-rest of this package.  Weights follow torch.nn.Linear's layout: W [out_features,
+rest of this package.  With Wk, Wv of H_kv * d_k rows (H_kv dividing n_heads) the
+attention is grouped-query (``gqa.py``); H_kv = n_heads is the plain layer.  Weights follow torch.nn.Linear's layout: W [out_features,
 in_features].  ``bpt_layer_fwd`` computes the whole sequence at once;
 ``bpt_layer_fwd_blocked`` follows the page's loop over query blocks and is used by the
 tests to show that the two agree (the fusion changes memory, not the result).
@@ -41,6 +42,7 @@ import math
 import numpy as np
 
 from .attention import attention_fwd
+from .gqa import gqa_bwd, gqa_fwd
 
 LN_EPS = 1e-5
 
@@ -72,6 +74,11 @@ def _heads(t, n_heads):
     return t.reshape(B, L, n_heads, d // n_heads)
 
 
+def _kv_heads(w, d, n_heads):
+    """Key/value heads: Wk is [H_kv * d_k, d] (grouped-query attention when H_kv < H)."""
+    return w["wk"].shape[0] // (d // n_heads)
+
+
 def _post_attention(xb, ab, w):
     """Output projection, residual, LN1, FFN, residual, LN2 for rows xb with attention ab."""
     h1 = layer_norm(xb + linear(ab, w["wo"], w["bo"]), w["ln1_g"], w["ln1_b"])
@@ -82,10 +89,11 @@ def _post_attention(xb, ab, w):
 def bpt_layer_fwd(x, w, n_heads, causal):
     """x [B, L, d] float64, w dict of float64 arrays (WEIGHT_NAMES).  Returns [B, L, d]."""
     B, L, d = x.shape
+    hkv = _kv_heads(w, d, n_heads)
     q = _heads(linear(x, w["wq"], w["bq"]), n_heads)
-    k = _heads(linear(x, w["wk"], w["bk"]), n_heads)
-    v = _heads(linear(x, w["wv"], w["bv"]), n_heads)
-    a, _ = attention_fwd(q, k, v, causal)
+    k = _heads(linear(x, w["wk"], w["bk"]), hkv)
+    v = _heads(linear(x, w["wv"], w["bv"]), hkv)
+    a, _ = gqa_fwd(q, k, v, causal)
     return _post_attention(x, a.reshape(B, L, d), w)
 
 
@@ -95,8 +103,9 @@ def bpt_layer_fwd_blocked(x, w, n_heads, causal, block_size):
     if L % block_size:
         raise ValueError("seq_len must be a multiple of block_size")
     q = linear(x, w["wq"], w["bq"])
-    k = _heads(linear(x, w["wk"], w["bk"]), n_heads)
-    v = _heads(linear(x, w["wv"], w["bv"]), n_heads)
+    hkv = _kv_heads(w, d, n_heads)
+    k = np.repeat(_heads(linear(x, w["wk"], w["bk"]), hkv), n_heads // hkv, axis=2)
+    v = np.repeat(_heads(linear(x, w["wv"], w["bv"]), hkv), n_heads // hkv, axis=2)
     out = np.zeros_like(x)
     dk = d // n_heads
     for s in range(0, L, block_size):
@@ -123,8 +132,9 @@ def bpt_layer_rows(x, w, n_heads, causal, b, rows):
     rows = np.asarray(rows)
     last = int(rows.max()) + 1 if causal else L
     xb = x[b]
-    kk = linear(xb[:last], w["wk"], w["bk"]).reshape(last, n_heads, dk)
-    vv = linear(xb[:last], w["wv"], w["bv"]).reshape(last, n_heads, dk)
+    hkv = _kv_heads(w, d, n_heads)
+    kk = np.repeat(linear(xb[:last], w["wk"], w["bk"]).reshape(last, hkv, dk), n_heads // hkv, 1)
+    vv = np.repeat(linear(xb[:last], w["wv"], w["bv"]).reshape(last, hkv, dk), n_heads // hkv, 1)
     qq = linear(xb[rows], w["wq"], w["bq"]).reshape(len(rows), n_heads, dk)
     a = np.zeros((len(rows), n_heads, dk))
     for n, r in enumerate(rows):
@@ -164,12 +174,12 @@ def _linear_bwd(xin, w, dy):
 def bpt_layer_bwd(x, w, n_heads, causal, dout):
     """Gradients of sum(out * dout) for the layer of bpt_layer_fwd, by the chain rule:
     returns a dict with "x" and every name of WEIGHT_NAMES."""
-    from .attention import attention_bwd
     B, L, d = x.shape
+    hkv = _kv_heads(w, d, n_heads)
     q = _heads(linear(x, w["wq"], w["bq"]), n_heads)
-    k = _heads(linear(x, w["wk"], w["bk"]), n_heads)
-    v = _heads(linear(x, w["wv"], w["bv"]), n_heads)
-    a4, _ = attention_fwd(q, k, v, causal)
+    k = _heads(linear(x, w["wk"], w["bk"]), hkv)
+    v = _heads(linear(x, w["wv"], w["bv"]), hkv)
+    a4, _ = gqa_fwd(q, k, v, causal)
     a = a4.reshape(B, L, d)
     y1 = x + linear(a, w["wo"], w["bo"])
     h1 = layer_norm(y1, w["ln1_g"], w["ln1_b"])
@@ -184,10 +194,10 @@ def bpt_layer_bwd(x, w, n_heads, causal, dout):
     dh1 = dy2 + dh1_f
     dy1, g["ln1_g"], g["ln1_b"] = layer_norm_bwd(y1, w["ln1_g"], dh1)
     da, g["wo"], g["bo"] = _linear_bwd(a, w["wo"], dy1)
-    dq, dk, dv = attention_bwd(q, k, v, da.reshape(B, L, n_heads, d // n_heads), causal)
+    dq, dk, dv = gqa_bwd(q, k, v, da.reshape(B, L, n_heads, d // n_heads), causal)
     dx = dy1.copy()
     for t, wn, bn in ((dq, "wq", "bq"), (dk, "wk", "bk"), (dv, "wv", "bv")):
-        dxi, g[wn], g[bn] = _linear_bwd(x, w[wn], t.reshape(B, L, d))
+        dxi, g[wn], g[bn] = _linear_bwd(x, w[wn], t.reshape(B, L, -1))
         dx += dxi
     g["x"] = dx
     return g

@@ -18,10 +18,11 @@ import oracle
 from oracle import bpt as obpt
 
 
-def _weights(d, d_ff, seed):
+def _weights(d, d_ff, seed, d_kv=None):
     rng = np.random.default_rng(seed)
     w = {}
-    for name, (o, i) in (("wq", (d, d)), ("wk", (d, d)), ("wv", (d, d)), ("wo", (d, d)),
+    d_kv = d if d_kv is None else d_kv
+    for name, (o, i) in (("wq", (d, d)), ("wk", (d_kv, d)), ("wv", (d_kv, d)), ("wo", (d, d)),
                          ("w1", (d_ff, d)), ("w2", (d, d_ff))):
         w[name] = rng.standard_normal((o, i)) / math.sqrt(i)
         w["b" + name[1:]] = 0.1 * rng.standard_normal(o)
@@ -35,9 +36,10 @@ def _torch_layer(x, w, n_heads, causal):
     """The same layer from torch's library modules, float64."""
     d = x.shape[-1]
     d_ff = w["w1"].shape[0]
+    d_kv = w["wk"].shape[0]
     T = lambda a: torch.from_numpy(np.ascontiguousarray(a))   # noqa: E731
     lin = {}
-    for name, (o, i) in (("q", (d, d)), ("k", (d, d)), ("v", (d, d)), ("o", (d, d)),
+    for name, (o, i) in (("q", (d, d)), ("k", (d_kv, d)), ("v", (d_kv, d)), ("o", (d, d)),
                          ("1", (d_ff, d)), ("2", (d, d_ff))):
         m = torch.nn.Linear(i, o, dtype=torch.float64)
         with torch.no_grad():
@@ -53,10 +55,12 @@ def _torch_layer(x, w, n_heads, causal):
         lns.append(m)
     xt = T(x)
     B, L, _ = x.shape
-    split = lambda t: t.view(B, L, n_heads, d // n_heads).transpose(1, 2)   # noqa: E731
+    dk = d // n_heads
+    split = lambda t: t.view(B, L, t.shape[-1] // dk, dk).transpose(1, 2)   # noqa: E731
     with torch.no_grad():
         a = F.scaled_dot_product_attention(split(lin["q"](xt)), split(lin["k"](xt)),
-                                           split(lin["v"](xt)), is_causal=causal)
+                                           split(lin["v"](xt)), is_causal=causal,
+                                           enable_gqa=d_kv != d)
         a = a.transpose(1, 2).reshape(B, L, d)
         h1 = lns[0](xt + lin["o"](a))
         f = lin["2"](torch.nn.GELU()(lin["1"](h1)))
@@ -64,10 +68,11 @@ def _torch_layer(x, w, n_heads, causal):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("B,L,d,H,d_ff", [(1, 64, 32, 2, 64), (2, 96, 48, 3, 96),
-                                          (1, 128, 64, 1, 256)])
-def test_layer_matches_library_modules(causal, B, L, d, H, d_ff):
-    w = _weights(d, d_ff, seed=L + d)
+@pytest.mark.parametrize("B,L,d,H,d_ff,Hkv", [(1, 64, 32, 2, 64, 2), (2, 96, 48, 3, 96, 3),
+                                              (1, 128, 64, 1, 256, 1), (1, 64, 64, 4, 128, 2),
+                                              (2, 48, 32, 4, 64, 1)])
+def test_layer_matches_library_modules(causal, B, L, d, H, d_ff, Hkv):
+    w = _weights(d, d_ff, seed=L + d, d_kv=Hkv * (d // H))
     x = np.random.default_rng(L).standard_normal((B, L, d))
     got = oracle.bpt_layer_fwd(x, w, H, causal)
     want = _torch_layer(x, w, H, causal)
@@ -76,8 +81,9 @@ def test_layer_matches_library_modules(causal, B, L, d, H, d_ff):
 
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("block", [16, 32, 128])
-def test_blockwise_loop_equals_whole_sequence(causal, block):
-    w = _weights(32, 64, seed=3)
+@pytest.mark.parametrize("d_kv", [32, 16])
+def test_blockwise_loop_equals_whole_sequence(causal, block, d_kv):
+    w = _weights(32, 64, seed=3, d_kv=d_kv)
     x = np.random.default_rng(4).standard_normal((2, 128, 32))
     a = oracle.bpt_layer_fwd(x, w, 2, causal)
     b = oracle.bpt_layer_fwd_blocked(x, w, 2, causal, block)
@@ -85,8 +91,9 @@ def test_blockwise_loop_equals_whole_sequence(causal, block):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_sampled_rows_equal_the_whole_layer(causal):
-    w = _weights(64, 128, seed=8)
+@pytest.mark.parametrize("d_kv", [64, 32])
+def test_sampled_rows_equal_the_whole_layer(causal, d_kv):
+    w = _weights(64, 128, seed=8, d_kv=d_kv)
     x = np.random.default_rng(9).standard_normal((2, 96, 64))
     full = oracle.bpt_layer_fwd(x, w, 2, causal)
     rows = [0, 1, 37, 95]
@@ -138,9 +145,10 @@ def test_planted_mistakes_fail_the_library_pin(monkeypatch):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_layer_backward_matches_torch_autograd(causal):
-    B, L, d, H, d_ff = 2, 48, 32, 2, 64
-    w = _weights(d, d_ff, seed=11)
+@pytest.mark.parametrize("Hkv", [4, 2, 1])
+def test_layer_backward_matches_torch_autograd(causal, Hkv):
+    B, L, d, H, d_ff = 2, 48, 32, 4, 64
+    w = _weights(d, d_ff, seed=11, d_kv=Hkv * (d // H))
     x = np.random.default_rng(12).standard_normal((B, L, d))
     dout = np.random.default_rng(13).standard_normal((B, L, d))
     got = oracle.bpt_layer_bwd(x, w, H, causal, dout)
@@ -148,10 +156,10 @@ def test_layer_backward_matches_torch_autograd(causal):
     T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).requires_grad_(True)   # noqa: E731
     wt = {k: T(v) for k, v in w.items()}
     xt = T(x)
-    split = lambda t: t.view(B, L, H, d // H).transpose(1, 2)   # noqa: E731
+    split = lambda t: t.view(B, L, t.shape[-1] // (d // H), d // H).transpose(1, 2)   # noqa: E731
     lin = lambda t, n: F.linear(t, wt["w" + n], wt["b" + n])     # noqa: E731
     a = F.scaled_dot_product_attention(split(lin(xt, "q")), split(lin(xt, "k")),
-                                       split(lin(xt, "v")), is_causal=causal)
+                                       split(lin(xt, "v")), is_causal=causal, enable_gqa=Hkv != H)
     a = a.transpose(1, 2).reshape(B, L, d)
     h1 = F.layer_norm(xt + lin(a, "o"), (d,), wt["ln1_g"], wt["ln1_b"], 1e-5)
     y = F.layer_norm(h1 + lin(F.gelu(lin(h1, "1")), "2"), (d,), wt["ln2_g"], wt["ln2_b"], 1e-5)
