@@ -341,13 +341,36 @@ def ra_layernorm(x, gamma, beta, eps=1e-5, out_dtype=torch.bfloat16, stream=None
 
 
 def make_bpt_params(batch, seq_len, heads, head_dim, d_ff, P, block, layout="contiguous",
-                    causal=True, block_rows=0, ln_eps=0.0, n_split=0):
+                    causal=True, block_rows=0, ln_eps=0.0, n_split=0, kv_heads=0):
     return BptParams(make_params(batch, seq_len, heads, head_dim, P, block, layout, causal, 0.0,
-                                 n_split, 0), int(d_ff), int(block_rows), float(ln_eps))
+                                 n_split, kv_heads), int(d_ff), int(block_rows), float(ln_eps))
 
 
 def bpt_workspace_bytes(params):
     return lib().ra_bpt_workspace_bytes(ctypes.byref(params))
+
+
+def _bpt_params_of(x, weights, heads, P, block, layout, causal, block_rows):
+    """Check the layer's parameter tensors and build its ra_bpt_params_t; the number of
+    key/value heads follows from wk's shape [H_kv * head_dim, d]."""
+    B, L, d = x.shape
+    hd = d // heads
+    for n in BPT_WEIGHTS:
+        if n not in weights:
+            raise ValueError("missing layer parameter %r" % n)
+    d_ff = weights["w1"].shape[0]
+    d_kv = weights["wk"].shape[0]
+    shapes = {"wq": (d, d), "wk": (d_kv, d), "wv": (d_kv, d), "wo": (d, d), "w1": (d_ff, d),
+              "w2": (d, d_ff), "bq": (d,), "bk": (d_kv,), "bv": (d_kv,), "bo": (d,),
+              "b1": (d_ff,), "b2": (d,), "ln1_g": (d,), "ln1_b": (d,), "ln2_g": (d,),
+              "ln2_b": (d,)}
+    for n in BPT_WEIGHTS:
+        _want(weights[n], torch.bfloat16 if n[0] == "w" else torch.float32, n, shapes[n],
+              x.device)
+    if d_kv % hd or heads % (d_kv // hd):
+        raise ValueError("wk has %d rows: not a divisor of the heads times head_dim %d" % (d_kv, hd))
+    return make_bpt_params(B, L, heads, hd, d_ff, P, block, layout, causal, block_rows,
+                           kv_heads=d_kv // hd)
 
 
 def bpt_train_workspace_bytes(params):
@@ -361,16 +384,7 @@ def ra_bpt_fwd(x, weights, heads, P, block, layout="contiguous", causal=True, bl
     train=True sizes the workspace for a following ra_bpt_bwd, which reuses it."""
     B, L, d = x.shape
     _want(x, torch.bfloat16, "x")
-    d_ff = weights["w1"].shape[0]
-    shapes = {"wq": (d, d), "wk": (d, d), "wv": (d, d), "wo": (d, d), "w1": (d_ff, d),
-              "w2": (d, d_ff), "bq": (d,), "bk": (d,), "bv": (d,), "bo": (d,), "b1": (d_ff,),
-              "b2": (d,), "ln1_g": (d,), "ln1_b": (d,), "ln2_g": (d,), "ln2_b": (d,)}
-    for n in BPT_WEIGHTS:
-        if n not in weights:
-            raise ValueError("missing layer parameter %r" % n)
-        _want(weights[n], torch.bfloat16 if n[0] == "w" else torch.float32, n, shapes[n],
-              x.device)
-    prm = make_bpt_params(B, L, heads, d // heads, d_ff, P, block, layout, causal, block_rows)
+    prm = _bpt_params_of(x, weights, heads, P, block, layout, causal, block_rows)
     w = BptWeights(*[weights[n].data_ptr() for n in BPT_WEIGHTS])
     if out is None:
         out = torch.empty((B, L, d), dtype=out_dtype, device=x.device)
@@ -388,11 +402,9 @@ def ra_bpt_bwd(x, weights, dout, heads, P, block, layout="contiguous", causal=Tr
     """Gradients of the layer through ra_bpt_bwd, after ra_bpt_fwd(..., train=True) with the
     same workspace.  Returns a dict: "x" (bf16, like x) and every name of BPT_WEIGHTS
     (fp32, shaped like the parameter)."""
-    B, L, d = x.shape
     _want(x, torch.bfloat16, "x")
     _want(dout, torch.bfloat16, "dout", tuple(x.shape), x.device)
-    d_ff = weights["w1"].shape[0]
-    prm = make_bpt_params(B, L, heads, d // heads, d_ff, P, block, layout, causal, block_rows)
+    prm = _bpt_params_of(x, weights, heads, P, block, layout, causal, block_rows)
     w = BptWeights(*[weights[n].data_ptr() for n in BPT_WEIGHTS])
     grads = {"x": torch.empty_like(x)}
     for n in BPT_WEIGHTS:

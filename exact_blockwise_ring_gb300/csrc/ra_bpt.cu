@@ -91,14 +91,15 @@ bool bpt_layout(const ra_bpt_params_t* p, BptWs* w) {
   if (attn_b > attn) attn = attn_b;
   const int64_t rows = (int64_t)a->batch * a->seq_len;
   const int64_t d = (int64_t)a->heads * a->head_dim;
+  const int64_t dkv = (int64_t)(a->kv_heads > 0 ? a->kv_heads : a->heads) * a->head_dim;
   int64_t R = p->block_rows > 0 ? p->block_rows : (rows < 16384 ? rows : 16384);
   if (R > rows) R = rows;
   w->R = R;
   size_t off = r256(attn);
   w->attn = 0;
   w->q = off; off += r256((size_t)rows * d * 2);
-  w->k = off; off += r256((size_t)rows * d * 2);
-  w->v = off; off += r256((size_t)rows * d * 2);
+  w->k = off; off += r256((size_t)rows * dkv * 2);
+  w->v = off; off += r256((size_t)rows * dkv * 2);
   w->a = off; off += r256((size_t)rows * d * 2);
   w->lse = off; off += r256((size_t)a->batch * a->heads * a->seq_len * 4);
   w->y = off; off += r256((size_t)R * d * 4);
@@ -113,8 +114,8 @@ bool bpt_layout(const ra_bpt_params_t* p, BptWs* w) {
   w->da = off; off += r256((size_t)rows * d * 2);
   w->dxa = off; off += r256((size_t)rows * d * 4);
   w->dq = off; off += r256((size_t)rows * d * 2);
-  w->dk = off; off += r256((size_t)rows * d * 2);
-  w->dv = off; off += r256((size_t)rows * d * 2);
+  w->dk = off; off += r256((size_t)rows * dkv * 2);
+  w->dv = off; off += r256((size_t)rows * dkv * 2);
   w->total_train = off;
   return true;
 }
@@ -126,10 +127,11 @@ ra_status_t cuda_err(cudaError_t e, const char* what) {
 ra_status_t check_bpt(const ra_bpt_params_t* p) {
   if (!p) return bfail(RA_ERR_INVALID_ARG, "params is NULL");
   const ra_params_t* a = &p->attn;
-  if (a->kv_heads != 0 && a->kv_heads != a->heads)
-    return bfail(RA_ERR_INVALID_ARG, "the layer projects K and V to all heads: kv_heads must be 0");
   if (ra_fwd_workspace_bytes(a) == 0)
     return bfail(RA_ERR_INVALID_ARG, "invalid attention parameters (see ra_fwd)");
+  const long long dkv = (long long)(a->kv_heads > 0 ? a->kv_heads : a->heads) * a->head_dim;
+  if (dkv % 256 != 0)
+    return bfail(RA_ERR_UNSUPPORTED, "kv_heads * head_dim (%lld) must be a multiple of 256", dkv);
   const long long d = (long long)a->heads * a->head_dim;
   if (d % 512 != 0 || d > 8192)
     return bfail(RA_ERR_UNSUPPORTED, "d_model = heads * head_dim (%lld) must be a multiple of 512 "
@@ -223,10 +225,12 @@ ra_status_t ra_bpt_fwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
   float* Y = reinterpret_cast<float*>(ws + w.y);
   void *H1 = ws + w.h1, *F = ws + w.f;
 
-  // projections over the whole sequence: [B*L, d] rows are [B, L, H, D] tensors
+  // projections over the whole sequence: [B*L, d] rows are [B, L, H, D] tensors (K and V
+  // [B, L, H_kv, D])
+  const int dkv = (a->kv_heads > 0 ? a->kv_heads : a->heads) * a->head_dim;
   if ((s = run_linear(rows, d, d, x, wt->wq, wt->bq, nullptr, RA_EPI_BIAS, Q, err, st)) != RA_OK ||
-      (s = run_linear(rows, d, d, x, wt->wk, wt->bk, nullptr, RA_EPI_BIAS, K, err, st)) != RA_OK ||
-      (s = run_linear(rows, d, d, x, wt->wv, wt->bv, nullptr, RA_EPI_BIAS, V, err, st)) != RA_OK)
+      (s = run_linear(rows, d, dkv, x, wt->wk, wt->bk, nullptr, RA_EPI_BIAS, K, err, st)) != RA_OK ||
+      (s = run_linear(rows, d, dkv, x, wt->wv, wt->bv, nullptr, RA_EPI_BIAS, V, err, st)) != RA_OK)
     return s;
   // ring attention; its workspace is the first part of this one (same error word)
   if ((s = ra_fwd(a, Q, K, V, A, RA_BF16, lse, nullptr, ws + w.attn, w.q, stream)) != RA_OK)
@@ -294,6 +298,7 @@ ra_status_t ra_bpt_bwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
   const int64_t rows = (int64_t)a->batch * a->seq_len;
   const int d = a->heads * a->head_dim;
   const int d_ff = p->d_ff;
+  const int dkv = (a->kv_heads > 0 ? a->kv_heads : a->heads) * a->head_dim;
   const float eps = p->ln_eps > 0.f ? p->ln_eps : 1e-5f;
   const uint8_t* xb = static_cast<const uint8_t*>(x);
   const uint8_t* dob = static_cast<const uint8_t*>(dout);
@@ -309,7 +314,7 @@ ra_status_t ra_bpt_bwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
   // gradients accumulated over blocks start at zero
   struct { float* p; size_t n; } acc[] = {
       {gr->wo, (size_t)d * d}, {gr->w1, (size_t)d_ff * d}, {gr->w2, (size_t)d * d_ff},
-      {gr->bq, (size_t)d}, {gr->bk, (size_t)d}, {gr->bv, (size_t)d}, {gr->bo, (size_t)d},
+      {gr->bq, (size_t)d}, {gr->bk, (size_t)dkv}, {gr->bv, (size_t)dkv}, {gr->bo, (size_t)d},
       {gr->b1, (size_t)d_ff}, {gr->b2, (size_t)d}, {gr->ln1_g, (size_t)d},
       {gr->ln1_b, (size_t)d}, {gr->ln2_g, (size_t)d}, {gr->ln2_b, (size_t)d}};
   for (auto& z : acc)
@@ -373,11 +378,12 @@ ra_status_t ra_bpt_bwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
   float* gw[3] = {gr->wq, gr->wk, gr->wv};
   float* gb[3] = {gr->bq, gr->bk, gr->bv};
   for (int t = 0; t < 3; ++t) {
-    if ((s = run_gemm(rows, d, d, dqkv[t], 0, wqkv[t], 1, nullptr, DXA, kEpiAddF32, DXA, err,
+    const int n_out = t == 0 ? d : dkv;          // Q is d wide, K and V H_kv * D
+    if ((s = run_gemm(rows, d, n_out, dqkv[t], 0, wqkv[t], 1, nullptr, DXA, kEpiAddF32, DXA, err,
                       st)) != RA_OK ||
-        (s = run_gemm(d, d, (int)rows, dqkv[t], 1, x, 1, nullptr, nullptr, kEpiPlainF32, gw[t],
-                      err, st)) != RA_OK ||
-        (s = cuda_err(launch_colsum(dqkv[t], 0, rows, d, gb[t], st), "column sum")) != RA_OK)
+        (s = run_gemm(n_out, d, (int)rows, dqkv[t], 1, x, 1, nullptr, nullptr, kEpiPlainF32,
+                      gw[t], err, st)) != RA_OK ||
+        (s = cuda_err(launch_colsum(dqkv[t], 0, rows, n_out, gb[t], st), "column sum")) != RA_OK)
       return s;
   }
   return cuda_err(launch_dq_convert(DXA, gr->dx, 1.0f, (size_t)rows * d, st), "dx convert");

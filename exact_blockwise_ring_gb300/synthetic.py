@@ -57,20 +57,21 @@ def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=T
     return tuple(out)
 
 
-def make_bpt_weights(d, d_ff, seed, device="cpu"):
+def make_bpt_weights(d, d_ff, seed, device="cpu", d_kv=None):
     """Random parameters of one blockwise transformer layer: Linear weights [out, in] drawn
     N(0, 1/in) and rounded to bf16, biases N(0, 0.01) fp32, LayerNorm scales 1 + N(0, 0.01)
     and shifts N(0, 0.01) fp32 (N(mean, variance)), drawn in the order wq, wk, wv, wo, w1, w2,
     bq, bk, bv, bo, b1, b2, ln1 scale, ln1 shift, ln2 scale, ln2 shift."""
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
-    shapes = {"wq": (d, d), "wk": (d, d), "wv": (d, d), "wo": (d, d), "w1": (d_ff, d),
+    d_kv = d if d_kv is None else d_kv        # K, V projection width (grouped-query: < d)
+    shapes = {"wq": (d, d), "wk": (d_kv, d), "wv": (d_kv, d), "wo": (d, d), "w1": (d_ff, d),
               "w2": (d, d_ff)}
     w = {}
     for name, (o, i) in shapes.items():
         x = torch.randn((o, i), generator=g, device=device, dtype=torch.float32) / (i ** 0.5)
         w[name] = x.to(torch.bfloat16)
-    for name, n in (("bq", d), ("bk", d), ("bv", d), ("bo", d), ("b1", d_ff), ("b2", d)):
+    for name, n in (("bq", d), ("bk", d_kv), ("bv", d_kv), ("bo", d), ("b1", d_ff), ("b2", d)):
         w[name] = 0.1 * torch.randn(n, generator=g, device=device, dtype=torch.float32)
     for ln in ("ln1", "ln2"):
         w[ln + "_g"] = 1.0 + 0.1 * torch.randn(d, generator=g, device=device, dtype=torch.float32)

@@ -271,8 +271,10 @@ ra_status_t ra_layernorm(int64_t rows, int features, const float* x, const float
 /*
  * Layer description.
  *   attn        the attention: batch, seq_len, heads, head_dim (d_model = heads *
- *               head_dim), block, P, layout, causal, softmax_scale, n_split as for ra_fwd;
- *               kv_heads must be 0 or heads (all three projections are d_model wide).
+ *               head_dim), block, P, layout, causal, softmax_scale, n_split, kv_heads as
+ *               for ra_fwd.  With kv_heads = H_kv < heads the K and V projections are
+ *               H_kv * head_dim wide (grouped-query attention); H_kv * head_dim must be a
+ *               multiple of 256.
  *   d_ff        feed-forward width, a multiple of 256.
  *   block_rows  rows of the flattened [batch * seq_len] sequence per post-attention
  *               block, a multiple of 128; 0 = min(batch * seq_len, 16384).
@@ -287,8 +289,8 @@ typedef struct {
 } ra_bpt_params_t;
 
 /* Layer parameters, all device pointers: weights bf16 in torch.nn.Linear layout
- * [out, in] (wq, wk, wv, wo [d, d]; w1 [d_ff, d]; w2 [d, d_ff]), biases and LayerNorm
- * scales / shifts fp32. */
+ * [out, in] (wq, wo [d, d]; wk, wv [H_kv * head_dim, d]; w1 [d_ff, d]; w2 [d, d_ff]),
+ * biases and LayerNorm scales / shifts fp32. */
 typedef struct {
   const void* wq;
   const void* wk;

@@ -184,7 +184,9 @@ def test_layernorm_rejects_bad_arguments(L):
     (dict(heads=2), False),                 # d_model 256: not a multiple of 512
     (dict(d_ff=1000), False),
     (dict(block_rows=100), False),
-    (dict(kv_heads=2), False),
+    (dict(kv_heads=2), True),               # grouped-query: K, V 256 wide
+    (dict(kv_heads=1), False),              # K, V 128 wide: not a multiple of 256
+    (dict(kv_heads=3), False),              # not a divisor of heads
     (dict(seq_len=1000), False),            # invalid attention parameters
 ])
 def test_bpt_workspace_bytes_validates(L, kw, ok):
@@ -199,7 +201,8 @@ def test_bpt_workspace_bytes_validates(L, kw, ok):
     if ok:
         d = base["heads"] * base["head_dim"]
         rows = base["batch"] * base["seq_len"]
-        assert n >= 4 * rows * d * 2 + base["block_rows"] * (d * 6 + base["d_ff"] * 2)
+        dkv = (base["kv_heads"] or base["heads"]) * base["head_dim"]
+        assert n >= (2 * d + 2 * dkv) * rows * 2 + base["block_rows"] * (d * 6 + base["d_ff"] * 2)
     else:
         assert n == 0
 

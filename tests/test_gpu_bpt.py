@@ -136,11 +136,11 @@ def test_bpt_fullsize_sampled_rows():
     assert np.all(np.abs(err) <= 5e-2 + 2.0 ** -8 * np.abs(ref))
 
 
-def _layer_grads_case(B, L, H, d_ff, seed):
+def _layer_grads_case(B, L, H, d_ff, seed, Hkv=None):
     d = H * 128
     x = make_inputs(B, L, 1, d, seed, with_dout=False)[0].view(B, L, d)
     dout = make_inputs(B, L, 1, d, seed + 1, with_dout=False)[0].view(B, L, d)
-    w = make_bpt_weights(d, d_ff, seed + 2)
+    w = make_bpt_weights(d, d_ff, seed + 2, d_kv=None if Hkv is None else Hkv * 128)
     ref = oracle.bpt_layer_bwd(_f64(x), {k: _f64(v) for k, v in w.items()}, H, True, _f64(dout))
     return x, dout, w, ref
 
@@ -224,3 +224,28 @@ def test_bpt_backward_fullsize_identities():
     assert float(g["bk"].norm()) <= 2e-2 * float(g["bv"].norm())
     for n, t in g.items():
         assert torch.isfinite(t).all(), n
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "striped"])
+def test_bpt_grouped_query_layer(layout):
+    """K and V projected to 2 heads for 4 query heads: forward and backward against the
+    oracle's layer with grouped-query attention."""
+    B, L, H, Hkv, d_ff, P = 1, 1024, 4, 2, 1024, 4
+    x, dout, w, ref = _layer_grads_case(B, L, H, d_ff, seed=95, Hkv=Hkv)
+    w64 = {k: _f64(v) for k, v in w.items()}
+    out_ref = oracle.bpt_layer_fwd(_f64(x), w64, H, True)
+    wd = {k: v.cuda() for k, v in w.items()}
+    ws = era.Workspace("cuda")
+    out = era.ra_bpt_fwd(x.cuda(), wd, H, P, 128, layout, True, block_rows=512, workspace=ws,
+                         out_dtype=torch.float32, train=True)
+    g = era.ra_bpt_bwd(x.cuda(), wd, dout.cuda(), H, P, 128, layout, True, block_rows=512,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    ws.check()
+    eo = _f64(out) - out_ref
+    assert np.linalg.norm(eo) / np.linalg.norm(out_ref) <= 1e-2 and np.max(np.abs(eo)) <= 5e-2
+    assert g["wk"].shape == w["wk"].shape and g["bv"].shape == w["bv"].shape
+    errs = {n: float(np.linalg.norm(_f64(g[n]) - ref[n]) / np.linalg.norm(ref[n]))
+            for n in ["x"] + [n for n in era.BPT_WEIGHTS if n != "bk"]}
+    assert max(errs.values()) <= 2e-2, errs
+    assert float(np.linalg.norm(_f64(g["bk"]))) <= 2e-2 * float(np.linalg.norm(ref["bv"]))
