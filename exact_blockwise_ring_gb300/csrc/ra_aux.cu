@@ -26,10 +26,13 @@ __device__ __forceinline__ void store4(void* out, int out_fp32, size_t elem, flo
   }
 }
 
-// Merge of n_parts normalised partials.  A row (b, token, h) is handled by `lpr` lanes
-// (D/8 rounded up to a power of two), each owning 8 consecutive features.  The partial
-// outputs of the first kPrefetch parts are loaded before the lse pass, so that their DRAM
-// latency overlaps the lse loads instead of following them; further parts stream after.
+// Merge of n_parts normalised partials.  Rows are taken in the order of the lse arrays,
+// (b, h) major and token fastest, so that the lse values of neighbouring rows are
+// neighbouring words (coalesced loads and stores) while each row's D outputs stay one
+// contiguous run.  A row is handled by `lpr` lanes (D/8 rounded up to a power of two),
+// each owning 8 consecutive features; the grid is capped and strides over the rows.  The
+// first kPrefetch parts' outputs and lse values are loaded before any is used, so their
+// DRAM latency overlaps; further parts stream after.
 constexpr int kPrefetch = 4;
 
 __global__ void __launch_bounds__(256)
@@ -37,65 +40,71 @@ __global__ void __launch_bounds__(256)
                  const float* __restrict__ lse_parts, int B, long long L, int H, int D, int lpr,
                  void* out, int out_fp32, float* lse) {
   const long long rows = (long long)B * L * H;
-  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / lpr;
+  const int rpb = 256 / lpr;                      // rows per block and pass
   const int sub = threadIdx.x % lpr;
-  if (row >= rows) return;
   const bool act = 8 * sub < D;
-  const int h = (int)(row % H);
-  const long long bl = row / H;
-  const long long tok = bl % L;
-  const int b = (int)(bl / L);
-  const size_t lidx = ((size_t)b * H + h) * L + tok;
   const size_t part_o = (size_t)rows * D;
-  const size_t part_l = (size_t)B * H * L;
-  const size_t e = (size_t)row * D + 8 * sub;
-  float4 pa[kPrefetch], pb[kPrefetch];
+  const size_t part_l = (size_t)rows;             // B * H * L
+  const long long step = (long long)gridDim.x * rpb;
+  for (long long r = (long long)blockIdx.x * rpb + threadIdx.x / lpr; r < rows; r += step) {
+    // r is the lse index (b * H + h) * L + token
+    const long long tok = r % L;
+    const long long bh = r / L;
+    const long long h = bh % H, b = bh / H;
+    const size_t e = (((size_t)b * L + tok) * H + h) * D + 8 * sub;
+    float4 pa[kPrefetch], pb[kPrefetch];
+    float lv[kPrefetch];
 #pragma unroll
-  for (int g = 0; g < kPrefetch; ++g) {
-    if (act && g < n_parts) {
-      const float4* src = reinterpret_cast<const float4*>(o_parts + g * part_o + e);
-      pa[g] = __ldg(src);
-      pb[g] = __ldg(src + 1);
-    } else {
-      pa[g] = pb[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  float mx = kNegInf;
-  for (int g = 0; g < n_parts; ++g) mx = fmaxf(mx, __ldg(lse_parts + g * part_l + lidx));
-  float tot = 0.f;
-  if (mx != kNegInf)
-    for (int g = 0; g < n_parts; ++g) {
-      const float l = __ldg(lse_parts + g * part_l + lidx);
-      if (l != kNegInf) tot += expf(l - mx);
-    }
-  const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  if (act) {
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-    if (tot > 0.f) {
-      // prefetched parts (static register indices), then the rest streamed
-#pragma unroll
-      for (int g = 0; g < kPrefetch; ++g) {
-        if (g >= n_parts) break;
-        const float l = __ldg(lse_parts + g * part_l + lidx);
-        if (l == kNegInf) continue;       // skipped, whatever its partial holds
-        const float w = expf(l - mx) * inv;
-        a0.x += w * pa[g].x; a0.y += w * pa[g].y; a0.z += w * pa[g].z; a0.w += w * pa[g].w;
-        a1.x += w * pb[g].x; a1.y += w * pb[g].y; a1.z += w * pb[g].z; a1.w += w * pb[g].w;
-      }
-      for (int g = kPrefetch; g < n_parts; ++g) {
-        const float l = __ldg(lse_parts + g * part_l + lidx);
-        if (l == kNegInf) continue;
-        const float w = expf(l - mx) * inv;
+    for (int g = 0; g < kPrefetch; ++g) {
+      if (act && g < n_parts) {
         const float4* src = reinterpret_cast<const float4*>(o_parts + g * part_o + e);
-        const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
-        a0.x += w * x0.x; a0.y += w * x0.y; a0.z += w * x0.z; a0.w += w * x0.w;
-        a1.x += w * x1.x; a1.y += w * x1.y; a1.z += w * x1.z; a1.w += w * x1.w;
+        pa[g] = __ldg(src);
+        pb[g] = __ldg(src + 1);
+      } else {
+        pa[g] = pb[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      lv[g] = g < n_parts ? __ldg(lse_parts + g * part_l + r) : kNegInf;
+    }
+    float mx = kNegInf;
+#pragma unroll
+    for (int g = 0; g < kPrefetch; ++g) mx = fmaxf(mx, lv[g]);
+    for (int g = kPrefetch; g < n_parts; ++g) mx = fmaxf(mx, __ldg(lse_parts + g * part_l + r));
+    float tot = 0.f;
+    if (mx != kNegInf) {
+#pragma unroll
+      for (int g = 0; g < kPrefetch; ++g)
+        if (lv[g] != kNegInf) tot += expf(lv[g] - mx);
+      for (int g = kPrefetch; g < n_parts; ++g) {
+        const float l = __ldg(lse_parts + g * part_l + r);
+        if (l != kNegInf) tot += expf(l - mx);
       }
     }
-    store4(out, out_fp32, e, a0);
-    store4(out, out_fp32, e + 4, a1);
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    if (act) {
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+      if (tot > 0.f) {
+#pragma unroll
+        for (int g = 0; g < kPrefetch; ++g) {
+          if (lv[g] == kNegInf) continue;   // skipped (or absent), whatever its partial holds
+          const float w = expf(lv[g] - mx) * inv;
+          a0.x += w * pa[g].x; a0.y += w * pa[g].y; a0.z += w * pa[g].z; a0.w += w * pa[g].w;
+          a1.x += w * pb[g].x; a1.y += w * pb[g].y; a1.z += w * pb[g].z; a1.w += w * pb[g].w;
+        }
+        for (int g = kPrefetch; g < n_parts; ++g) {
+          const float l = __ldg(lse_parts + g * part_l + r);
+          if (l == kNegInf) continue;
+          const float w = expf(l - mx) * inv;
+          const float4* src = reinterpret_cast<const float4*>(o_parts + g * part_o + e);
+          const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+          a0.x += w * x0.x; a0.y += w * x0.y; a0.z += w * x0.z; a0.w += w * x0.w;
+          a1.x += w * x1.x; a1.y += w * x1.y; a1.z += w * x1.z; a1.w += w * x1.w;
+        }
+      }
+      store4(out, out_fp32, e, a0);
+      store4(out, out_fp32, e + 4, a1);
+    }
+    if (sub == 0) lse[r] = tot > 0.f ? mx + logf(tot) : kNegInf;
   }
-  if (sub == 0) lse[lidx] = tot > 0.f ? mx + logf(tot) : kNegInf;
 }
 
 // Backward preprocess.  Per row (b, token, h):
@@ -214,8 +223,20 @@ cudaError_t launch_merge(int n_parts, const float* o_parts, const float* lse_par
   const long long rows = (long long)B * L * H;
   int lpr = 1;
   while (lpr < D / 8) lpr <<= 1;
-  merge_kernel<<<grid_for(rows, 256 / lpr), 256, 0, s>>>(n_parts, o_parts, lse_parts, B, L, H, D,
-                                                         lpr, out, out_fp32, lse);
+  // as many blocks as are resident at once (every SM full), striding over the rows
+  static int cap = 0;
+  if (cap == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_kernel, 256, 0) != cudaSuccess)
+      return cudaGetLastError();
+    cap = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  unsigned grid = grid_for(rows, 256 / lpr);
+  if (grid > (unsigned)cap) grid = (unsigned)cap;
+  merge_kernel<<<grid, 256, 0, s>>>(n_parts, o_parts, lse_parts, B, L, H, D, lpr, out, out_fp32,
+                                    lse);
   return cudaGetLastError();
 }
 
