@@ -146,14 +146,17 @@ def test_layouts_agree_and_runs_are_deterministic():
     assert float((lz - ls).abs().max()) <= LSE_TOL
 
 
-@pytest.mark.parametrize("n,D", [(3, 128), (6, 128), (1, 64), (5, 24), (2, 256)])
-def test_merge_entry_point_matches_oracle_merge(n, D):
+@pytest.mark.parametrize("n,D,B,L,H", [(3, 128, 1, 256, 2), (6, 128, 1, 256, 2), (1, 64, 1, 256, 2),
+                                       (5, 24, 1, 256, 2), (2, 256, 1, 256, 2),
+                                       (7, 128, 2, 384, 3), (4, 64, 3, 200, 5)])
+def test_merge_entry_point_matches_oracle_merge(n, D, B, L, H):
     rng = np.random.default_rng(3 + n + D)
-    B, L, H = 1, 256, 2
     o = rng.standard_normal((n, B, L, H, D)).astype(np.float32)
     lse = rng.standard_normal((n, B, H, L)).astype(np.float32)
     lse[n - 1, 0, 0, :7] = -np.inf
     o[n - 1, 0, :7, 0, :] = np.nan                  # a skipped partial's contents never matter
+    lse[0, B - 1, H - 1, L - 3:] = -np.inf          # skipped in the first part, at the tail
+    o[0, B - 1, L - 3:, H - 1, :] = np.nan
     lse[:, 0, 1, 5] = -np.inf                       # a row with no visible key at all
     o_or = np.where(np.isnan(o), 0.0, o).astype(np.float64)
     mo, ml = oracle.merge_partials(o_or, lse.astype(np.float64))
