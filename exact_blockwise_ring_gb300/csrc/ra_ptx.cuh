@@ -254,18 +254,11 @@ __device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr) {
   return sdesc_sw128(saddr, 16u, 1024u);
 }
 
-// MN-major operand (M or N contiguous inside a 128-byte row, K along rows).
-// mn_block_stride: bytes between consecutive 64-element MN blocks;
-// the 8-row K-group stride is 1024 bytes.
-#ifndef RA_MN_LBO_IS_MN
-#define RA_MN_LBO_IS_MN 1
-#endif
+// MN-major operand (M or N contiguous inside a 128-byte row, K along rows): the
+// leading-dimension offset is mn_block_stride, the bytes between consecutive 64-element
+// MN blocks; the stride-dimension offset is the 8-row K-group stride, 1024 bytes.
 __device__ __forceinline__ uint64_t sdesc_mnmajor(uint32_t saddr, uint32_t mn_block_stride) {
-#if RA_MN_LBO_IS_MN
   return sdesc_sw128(saddr, mn_block_stride, 1024u);
-#else
-  return sdesc_sw128(saddr, 1024u, mn_block_stride);
-#endif
 }
 
 // Instruction descriptor for tcgen05.mma kind::f16 with bf16 A/B and fp32 accumulate.
@@ -275,17 +268,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// Warpgroup register reallocation: the launch gives every thread the same count; the
-// producer/MMA warpgroup hands registers back and the math warpgroups take them.
-template <uint32_t N>
-__device__ __forceinline__ void reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void reg_alloc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- math -------------
