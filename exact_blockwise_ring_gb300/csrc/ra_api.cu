@@ -193,7 +193,9 @@ void work_model(const ra_params_t* p, unsigned long long* outp) {
         t += (unsigned long long)(Tb * Tb);
         pr += R * n;
       } else if (p->layout == RA_LAYOUT_STRIPED) {
-        t += (unsigned long long)(Tb * (Tb + 1) / 2);
+        // query block tb sees KV blocks u < tb and its diagonal u = tb; with one-token
+        // blocks the diagonal's only pair is masked when the KV shard comes later (j > i)
+        t += (unsigned long long)(Tb * (Tb + 1) / 2) - ((blk == 1 && j > i) ? (unsigned long long)Tb : 0ull);
         pr += (j <= i) ? sum_a + R : sum_a;
       } else {
         for (long long tb = 0; tb < Tb; ++tb)

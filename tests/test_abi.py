@@ -141,6 +141,23 @@ def test_work_model_matches_oracle(L, layout, causal, L_, P, block):
     assert got == want
 
 
+def test_work_model_matches_oracle_random_shapes(L):
+    # seeded sweep of small shapes: any P, any number of blocks per shard (zigzag: an even
+    # number), blocks of 1 to 16 tokens, every layout, causal or not
+    import random
+    rng = random.Random(20261202)
+    for _ in range(200):
+        layout = rng.choice(["contiguous", "striped", "zigzag"])
+        causal = rng.random() < 0.8
+        P = rng.randint(1, 9)
+        block = rng.choice([1, 2, 3, 4, 8, 16])
+        T = rng.randint(1, 6) * (2 if layout == "zigzag" else 1)
+        L_ = P * T * block
+        got = era.ra_shard_work_model(L_, P, block, layout, causal)
+        want = oracle.shard_work(L_, P, block, layout, causal)
+        assert got == want, (L_, P, block, layout, causal)
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "_lib", None)
     monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "libra.so"))
