@@ -121,7 +121,8 @@ size_t ra_bwd_workspace_bytes(const ra_params_t* p);
  *   lse          fp32 [B, H, L]; -inf for a row with no visible key.
  *   shard_work   NULL, or device uint64 [3][P] overwritten with the per-shard work the
  *                kernel executed: [0][i] (Q block, KV block) pairs of `block` tokens
- *                computed for the queries of shard i, [1][i] unmasked (query, key)
+ *                computed for the queries of shard i (causal: those holding at least
+ *                one visible (query, key) pair; all otherwise), [1][i] unmasked (query, key)
  *                pairs, [2][i] the vanos001 "Worked Demo" unit (per query row, KV
  *                blocks in natural order holding a visible key).
  *   workspace    device buffer of >= ra_fwd_workspace_bytes(p) bytes.
