@@ -99,31 +99,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// Query tiles of shard i that see KV tile (j, u): for query tile t (128 rows),
-//   key row b (0..127) is visible to query row a (0..127) iff a - b + delta >= 0 with
-//   contiguous, zigzag: delta = 128 (block_pos(i, t) - block_pos(j, u))
-//   striped:            delta = 128 (t - u) - (i < j)
-// skip: delta < -127; full: delta >= 127 (or non-causal); otherwise masked.  Tile
-// positions grow with t, so the visible query tiles of a shard are a suffix t >= t_lo.
-struct BwdSched {
-  int j, u, n, T, P, layout, causal;
-  __device__ int i_of(int k) const { return (j + k) % P; }
-  __device__ long long delta(int i, int t) const {
-    if (layout == RA_LAYOUT_STRIPED) return 128LL * (t - u) - (i < j ? 1 : 0);
-    return 128LL * (block_pos(layout, i, t, T, P) - block_pos(layout, j, u, T, P));
-  }
-  // first query tile with delta >= -127
-  __device__ int t_lo(int i) const {
-    if (!causal) return 0;
-    if (layout != RA_LAYOUT_STRIPED)
-      return (int)blocks_upto(layout, i, block_pos(layout, j, u, T, P) - 1, T, P);
-    const long long num = 128LL * u + (i < j ? 1 : 0) - 127;
-    if (num <= 0) return 0;
-    const long long t = (num + 127) / 128;
-    return t > T ? T : (int)t;
-  }
-};
-
 __global__ void __launch_bounds__(640, 1)
     ra_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,

@@ -1,5 +1,6 @@
 """The token-assignment and ring-schedule helpers the kernels share (csrc/ra_internal.h:
-token_of, shard_local_of, tokens_upto and RingSched's q_end / q_diag / u_end), compiled for
+token_of, shard_local_of, tokens_upto, RingSched's q_end / q_diag / u_end for the forward
+and BwdSched's t_lo / delta for the backward), compiled for
 the host and checked against brute force built on the oracle's token assignment
 (oracle/work.py) over a seeded sweep of small shapes, every layout, causal or not.
 
@@ -36,6 +37,20 @@ int main(int argc, char** argv) {
   const int layout = atoi(argv[1]), P = atoi(argv[2]);
   const long long n = atoll(argv[3]);
   const int T = atoi(argv[4]), causal = atoi(argv[5]);
+  if (argc > 6) {   // the backward's schedule (128-row tiles): t_lo, then delta per tile
+    printf("B");
+    for (int j = 0; j < P; ++j)
+      for (int u = 0; u < T; ++u) {
+        const BwdSched sc{j, u, (int)n, T, P, layout, causal};
+        for (int k = 0; k < P; ++k) {
+          const int i = sc.i_of(k);
+          printf(" %d %d", i, sc.t_lo(i));
+          for (int t = 0; t < T; ++t) printf(" %lld", sc.delta(i, t));
+        }
+      }
+    printf("\n");
+    return 0;
+  }
   printf("T");
   for (int i = 0; i < P; ++i)
     for (long long a = 0; a < n; ++a) printf(" %lld", token_of(layout, i, a, n, P));
@@ -128,6 +143,47 @@ def test_layout_helpers_match_brute_force(harness):
                     e1, d1 = _ring_ref(tokens, i, j, 2 * s + 1, T, bt, causal)
                     want_q += [e0, e1, d0, d1, max(e0, e1)]
         assert got["Q"] == want_q, (layout, P, T, bt, causal)
+
+
+def test_backward_schedule_matches_brute_force(harness):
+    # BwdSched with the kernels' 128-row tiles: the query shards come in ring order, the
+    # visible query tiles of a shard are a suffix t >= t_lo, and inside a tile pair key row
+    # b is visible to query row a exactly when a - b + delta >= 0
+    rows = [0, 1, 2, 63, 64, 65, 126, 127]
+    rng = random.Random(77)
+    for _ in range(24):
+        layout = rng.choice(list(LAYOUTS))
+        causal = rng.random() < 0.8
+        P = rng.randint(1, 5)
+        T = rng.randint(1, 3) * (2 if layout == "zigzag" else 1)
+        n = 128 * T
+        L = P * n
+        out = subprocess.run([harness, str(LAYOUTS[layout]), str(P), str(n), str(T),
+                              str(int(causal)), "bwd"], capture_output=True, text=True, timeout=60)
+        assert out.returncode == 0, out.stderr
+        vals = [int(x) for x in out.stdout.split()[1:]]
+        tokens = [shard_tokens(i, L, P, layout) for i in range(P)]
+        pos = 0
+        for j in range(P):
+            for u in range(T):
+                kt = tokens[j][u * 128:(u + 1) * 128]
+                for i in [(j + k) % P for k in range(P)]:     # i = (j + k) mod P
+                    gi, t_lo = vals[pos], vals[pos + 1]
+                    deltas = vals[pos + 2:pos + 2 + T]
+                    pos += 2 + T
+                    assert gi == i
+                    vis = [min(kt) <= max(tokens[i][t * 128:(t + 1) * 128]) if causal else True
+                           for t in range(T)]
+                    want_lo = vis.index(True) if True in vis else T
+                    assert vis == [False] * want_lo + [True] * (T - want_lo)
+                    assert t_lo == want_lo, (layout, P, T, j, u, i)
+                    if causal:
+                        for t in range(T):
+                            qt = tokens[i][t * 128:(t + 1) * 128]
+                            for a in rows:
+                                for b in rows:
+                                    assert (a - b + deltas[t] >= 0) == (kt[b] <= qt[a])
+        assert pos == len(vals)
 
 
 def test_planted_schedule_error_is_caught():
