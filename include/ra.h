@@ -88,6 +88,9 @@ typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype_t;
  *                    G = H / H_kv consecutive query heads share one; the gradient of a
  *                    shared head is the sum over its G query heads (labhub, comparison
  *                    section "比較分析": ring attention is fully compatible with GQA/MQA).
+ * Size limits: B * L * H * D <= 2^40 elements and B * H * L <= 2^36 rows.  A violated
+ * rule is RA_ERR_INVALID_ARG, except a head_dim or block outside the sets above
+ * (RA_ERR_UNSUPPORTED: a valid request with no kernel).
  */
 typedef struct {
   int batch;

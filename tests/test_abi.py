@@ -254,3 +254,56 @@ def test_bpt_train_workspace_and_backward_checks(L):
                         FAKE, 1 << 40, None) == 1
     assert L.ra_bpt_bwd(ctypes.byref(prm), FAKE, ctypes.byref(w), FAKE, ctypes.byref(gr), FAKE,
                         64, None) == 3
+
+
+def _documented_valid(B, L, H, D, blk, P, layout, causal, scale, n_split, kv):
+    """The rules ra.h states for ra_params_t, restated."""
+    if B < 1 or H < 1 or L < 1 or not 1 <= P <= 1024:
+        return False
+    if layout not in (0, 1, 2) or causal not in (0, 1):
+        return False
+    if D not in (64, 128) or blk not in (128, 256):
+        return False
+    if L % (P * blk) or (layout == 2 and L % (2 * P * blk)):
+        return False
+    if not (scale >= 0.0) or scale == float("inf"):
+        return False
+    if n_split < 0 or (n_split > 0 and P % n_split):
+        return False
+    if kv < 0 or (kv > 0 and H % kv):
+        return False
+    return B * L * H * D <= 1 << 40 and B * H * L <= 1 << 36
+
+
+def test_parameter_rules_match_the_header(L):
+    # seeded sweep over valid and invalid parameter sets: the library accepts exactly the
+    # ones the header's rules allow (workspace size 0 marks a rejected set)
+    import random
+    rng = random.Random(4242)
+    seen = {True: 0, False: 0}
+    def pick(good, bad, p_good=0.9):
+        return rng.choice(good) if rng.random() < p_good else rng.choice(bad)
+
+    for _ in range(3000):
+        P = pick([1, 2, 3, 4, 8, 16, 1024], [0, -1, 1025])
+        blk = pick([128, 256], [64, 100, 0])
+        layout = pick([0, 1, 2], [3, -1])
+        mult = rng.choice([1, 2, 3, 4, 6])
+        L_ = max(P, 1) * max(blk, 1) * mult
+        if rng.random() < 0.15:
+            L_ += rng.choice([1, 64, 128])
+        if rng.random() < 0.03:
+            L_ = rng.choice([0, -128, 1 << 34])
+        B = pick([1, 2, 3], [0, -1, 1 << 20])
+        H = pick([1, 2, 6, 32], [0, -4])
+        D = pick([64, 128], [96, 0, 256])
+        causal = pick([0, 1], [2, -1])
+        scale = pick([0.0, 0.125, 3.0], [-1.0, float("inf"), float("nan")])
+        n_split = pick([0, 1, 2, 4], [3, -1, 5])
+        kv = pick([0, 1, 2], [3, -2, 4, 5])
+        prm = api.Params(B, L_, H, D, blk, P, layout, causal, scale, n_split, kv)
+        want = _documented_valid(B, L_, H, D, blk, P, layout, causal, scale, n_split, kv)
+        got = api.fwd_workspace_bytes(prm) > 0
+        assert got == want, (B, L_, H, D, blk, P, layout, causal, scale, n_split, kv)
+        seen[want] += 1
+    assert seen[True] > 100 and seen[False] > 100
