@@ -279,10 +279,10 @@ ra_status_t ra_layernorm(int64_t rows, int features, const float* x, const float
  *               for ra_fwd.  With kv_heads = H_kv < heads the K and V projections are
  *               H_kv * head_dim wide (grouped-query attention); H_kv * head_dim must be a
  *               multiple of 256.
- *   d_ff        feed-forward width, a multiple of 256.
+ *   d_ff        feed-forward width, a positive multiple of 256.
  *   block_rows  rows of the flattened [batch * seq_len] sequence per post-attention
  *               block, a multiple of 128; 0 = min(batch * seq_len, 16384).
- *   ln_eps      LayerNorm epsilon, 0 = 1e-5.
+ *   ln_eps      LayerNorm epsilon (>= 0), 0 = 1e-5.
  * d_model must be a multiple of 512 and at most 8192.
  */
 typedef struct {

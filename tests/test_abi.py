@@ -307,3 +307,33 @@ def test_parameter_rules_match_the_header(L):
         assert got == want, (B, L_, H, D, blk, P, layout, causal, scale, n_split, kv)
         seen[want] += 1
     assert seen[True] > 100 and seen[False] > 100
+
+
+def test_layer_parameter_rules_match_the_header(L):
+    # the layer's own rules on top of the attention's (a valid attention part throughout):
+    # d_model % 512 == 0 and <= 8192, H_kv * head_dim % 256 == 0, d_ff a positive multiple
+    # of 256, block_rows 0 or a positive multiple of 128, ln_eps >= 0; the training
+    # workspace also needs head_dim 128 and d_model <= 4096
+    import random
+    rng = random.Random(515)
+    seen = {True: 0, False: 0}
+    for _ in range(1500):
+        D = rng.choice([64, 128])
+        H = rng.choice([1, 2, 4, 6, 8, 16, 32, 48, 64, 65, 96, 128])
+        kv = rng.choice([0, 0, 1, 2, 4, 8])
+        if kv and H % kv:
+            kv = 0
+        d_ff = rng.choice([256, 512, 4096, 16384, 0, 100, 300])
+        block_rows = rng.choice([0, 128, 256, 16384, 100, -128])
+        eps = rng.choice([0.0, 1e-5, 1e-6, -1.0, float("nan")])
+        attn = api.Params(1, 1024, H, D, 128, 4, 1, 1, 0.0, 0, kv)
+        prm = api.BptParams(attn, d_ff, block_rows, eps)
+        d, dkv = H * D, (kv or H) * D
+        want = (d % 512 == 0 and d <= 8192 and dkv % 256 == 0 and d_ff >= 256 and
+                d_ff % 256 == 0 and block_rows >= 0 and block_rows % 128 == 0 and eps >= 0.0)
+        assert (api.lib().ra_bpt_workspace_bytes(ctypes.byref(prm)) > 0) == want, (
+            H, D, kv, d_ff, block_rows, eps)
+        want_train = want and D == 128 and d <= 4096
+        assert (api.lib().ra_bpt_train_workspace_bytes(ctypes.byref(prm)) > 0) == want_train
+        seen[want] += 1
+    assert seen[True] > 50 and seen[False] > 50
