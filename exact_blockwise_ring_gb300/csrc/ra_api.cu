@@ -479,7 +479,6 @@ ra_status_t ra_merge(int n_parts, const float* o_parts, const float* lse_parts, 
   if (!aligned16(o_parts) || !aligned16(out)) return fail(RA_ERR_INVALID_ARG, "misaligned pointer");
   if (out_dtype != RA_BF16 && out_dtype != RA_FP32)
     return fail(RA_ERR_INVALID_ARG, "out_dtype must be RA_BF16 or RA_FP32");
-  if (head_dim % 4 != 0) return fail(RA_ERR_INVALID_ARG, "head_dim must be a multiple of 4");
   cudaError_t e = launch_merge(n_parts, o_parts, lse_parts, batch, seq_len, heads, head_dim, out,
                                out_dtype == RA_FP32, lse, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
