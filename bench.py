@@ -426,9 +426,26 @@ def run_ours(args, w, rank, world, local):
         torch.cuda.synchronize()
         ws.check()
         e_ms = dist_max(a0.elapsed_time(a1), world)
+        # this machine's host link, after the timed region: one step's copies each way
+        # alone, same pinned buffers and streams (explains an e2e gap to the device rate)
+        link = {}
+        din0, dout0, hout0, _ = sets[0]
+        for name, s_, pairs_, nb in (("h2d_gbs", s_up, list(zip(din0, hin)), h2d),
+                                     ("d2h_gbs", s_down, list(zip(hout0, dout0)), d2h)):
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s_):
+                c0.record(s_)
+                for dst, src in pairs_:
+                    dst.copy_(src, non_blocking=True)
+                c1.record(s_)
+            torch.cuda.synchronize()
+            link[name] = round(nb / (c0.elapsed_time(c1) * 1e-3) / 1e9, 1)
         e2e = {"value": round(job_rate(world, step_flops, K, e_ms), 2),
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e_ms / K, 3),
+               "host_link": link,
                "copies": "each step's H2D and D2H overlap the neighbouring steps' compute "
                          "(two buffer sets, two copy streams)"}
 
