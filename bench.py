@@ -415,17 +415,23 @@ def run_ours(args, w, rank, world, local):
         for sidx in range(2):
             e2e_step(sidx)
         torch.cuda.synchronize()
-        dist_barrier(world)
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(s_up)
-        for sidx in range(K):
-            e2e_step(sidx)
-        s_down.wait_stream(stream)
-        a1.record(s_down)
-        torch.cuda.synchronize()
+        # three timed windows of K steps each; the line reports the median window and lists
+        # all three (on a virtualised host a single host-memory copy can stall for ~100 ms,
+        # which one window of K steps cannot absorb)
+        windows = []
+        for _ in range(3):
+            dist_barrier(world)
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(s_up)
+            for sidx in range(K):
+                e2e_step(sidx)
+            s_down.wait_stream(stream)
+            a1.record(s_down)
+            torch.cuda.synchronize()
+            windows.append(dist_max(a0.elapsed_time(a1), world))
         ws.check()
-        e_ms = dist_max(a0.elapsed_time(a1), world)
+        e_ms = sorted(windows)[1]
         # this machine's host link, after the timed region: one step's copies each way
         # alone, same pinned buffers and streams (explains an e2e gap to the device rate)
         link = {}
@@ -445,9 +451,11 @@ def run_ours(args, w, rank, world, local):
         e2e = {"value": round(job_rate(world, step_flops, K, e_ms), 2),
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e_ms / K, 3),
+               "windows": [round(job_rate(world, step_flops, K, x), 2) for x in windows],
                "host_link": link,
                "copies": "each step's H2D and D2H overlap the neighbouring steps' compute "
-                         "(two buffer sets, two copy streams)"}
+                         "(two buffer sets, two copy streams); value = the median of three "
+                         "timed windows of K steps (all three in windows)"}
 
     # the bandwidth-bound kernels against the measured HBM copy rate: the backward's
     # preprocess and finalize (timed inside the steps above) and the partial merge (timed

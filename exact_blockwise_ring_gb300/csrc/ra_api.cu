@@ -354,8 +354,6 @@ ra_status_t bwd_common(const ra_params_t* p, void* workspace, size_t workspace_b
                        BwdWs* w) {
   ra_status_t s = check_params(p, true);
   if (s != RA_OK) return s;
-  if (p->head_dim != 128)
-    return fail(RA_ERR_UNSUPPORTED, "backward kernels exist for head_dim 128");
   const size_t need = bwd_ws(p);
   if (!workspace || workspace_bytes < need || !aligned16(workspace))
     return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,

@@ -262,7 +262,7 @@ ra_status_t ra_bpt_fwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
 
 size_t ra_bpt_train_workspace_bytes(const ra_bpt_params_t* p) {
   if (check_bpt(p) != RA_OK) return 0;
-  if (p->attn.head_dim != 128 || (long long)p->attn.heads * p->attn.head_dim > 4096) return 0;
+  if ((long long)p->attn.heads * p->attn.head_dim > 4096) return 0;
   BptWs w;
   return bpt_layout(p, &w) ? w.total_train : 0;
 }
@@ -272,8 +272,6 @@ ra_status_t ra_bpt_bwd(const ra_bpt_params_t* p, const void* x, const ra_bpt_wei
                        size_t workspace_bytes, void* stream) {
   ra_status_t s = check_bpt(p);
   if (s != RA_OK) return s;
-  if (p->attn.head_dim != 128)
-    return bfail(RA_ERR_UNSUPPORTED, "the layer's backward needs head_dim 128");
   if ((long long)p->attn.heads * p->attn.head_dim > 4096)
     return bfail(RA_ERR_UNSUPPORTED, "the layer's backward needs d_model <= 4096");
   if (!x || !wt || !dout || !gr) return bfail(RA_ERR_INVALID_ARG, "null pointer");

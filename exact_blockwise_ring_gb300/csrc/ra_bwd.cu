@@ -47,15 +47,19 @@ namespace {
 
 constexpr int BQ = 128;     // query rows per tile
 constexpr int NSTQ = 2;     // query-side pipeline stages
-constexpr int D_ = 128;     // head dim of this kernel
 
+// D_ = head dim (64 or 128).  K stays resident 128 features wide: with D_ = 64 its
+// features [64, 128) are zero, so that dQ^T = K^T dS^T keeps M = 128 (rows [64, 128) of
+// the product are zero and are not drained).
+template <int D_>
 struct BwdCfg {
-  static constexpr int KB = kTile * D_ * 2;        // K or V tile bytes (32 KB)
-  static constexpr int QB = BQ * D_ * 2;           // Q or dO tile bytes (32 KB)
+  static constexpr int KB = kTile * 128 * 2;       // K tile bytes in shared memory (32 KB)
+  static constexpr int VB = kTile * D_ * 2;        // V tile bytes, also the K bytes loaded
+  static constexpr int QB = BQ * D_ * 2;           // Q or dO tile bytes
   static constexpr int SB = kTile * BQ * 2;        // dS^T tile bytes (32 KB)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KB;
-  static constexpr int OFF_Q = OFF_V + KB;
+  static constexpr int OFF_Q = OFF_V + VB;
   static constexpr int OFF_DO = OFF_Q + NSTQ * QB;
   static constexpr int OFF_DS = OFF_DO + NSTQ * QB;
   static constexpr int OFF_LD = OFF_DS + SB;       // per stage: 128 lse2 + 128 D floats
@@ -67,7 +71,7 @@ struct BwdCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // no alignment slack: the kernel requires (and checks) a 1024-byte aligned base
   static constexpr int SMEM_BYTES = OFF_MISC + 64;
-  static constexpr int COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
+  static constexpr int COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D_;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -99,11 +103,12 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+template <int D_>
 __global__ void __launch_bounds__(640, 1)
     ra_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs a) {
-  using C = BwdCfg;
+  using C = BwdCfg<D_>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   uint8_t* sK = sm + C::OFF_K;
@@ -174,6 +179,13 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(drain, 1);
     fence_mbar_init();
   }
+  if constexpr (D_ < 128) {
+    // K's feature columns [D_, 128): zero for the dQ^T product (no TMA writes there)
+    uint4* pad = reinterpret_cast<uint4*>(sK + (D_ / 64) * kTile * 128);
+    for (int x = threadIdx.x; x < ((128 - D_) / 64) * kTile * 128 / 16; x += blockDim.x)
+      pad[x] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   __syncthreads();
   if (*abort_flag) return;   // an earlier CTA gave up: uniform early exit, nothing held
   if (warp == 1) {
@@ -192,8 +204,8 @@ __global__ void __launch_bounds__(640, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
-      mbar_expect_tx(kv_full, 2 * C::KB);
-      for (int cb = 0; cb < 2; ++cb) {
+      mbar_expect_tx(kv_full, 2 * C::VB);
+      for (int cb = 0; cb < D_ / 64; ++cb) {
         load_rows(sK + cb * kTile * 128, &tmK, kv_full, a.layout, cb * 64, hk, j, u * kTile, b,
                   a.n, a.P);
         load_rows(sV + cb * kTile * 128, &tmV, kv_full, a.layout, cb * 64, hk, j, u * kTile, b,
@@ -212,7 +224,7 @@ __global__ void __launch_bounds__(640, 1)
               break;
             }
             mbar_expect_tx(&q_full[st], 2 * C::QB + C::LDB);
-            for (int cb = 0; cb < 2; ++cb) {
+            for (int cb = 0; cb < D_ / 64; ++cb) {
               load_rows(sQ + st * C::QB + cb * BQ * 128, &tmQ, &q_full[st], a.layout, cb * 64, h, i,
                         t * BQ, b, a.n, a.P);
               load_rows(sDO + st * C::QB + cb * BQ * 128, &tmDO, &q_full[st], a.layout, cb * 64, h,
@@ -458,6 +470,7 @@ __global__ void __launch_bounds__(640, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(dq_empty);
+          if (drow >= D_) continue;   // a zero row of the padded K (D_ = 64)
           // 64 consecutive local rows: consecutive tokens (stride qstride) in every layout
           const long long tok0 = token_of(a.layout, i, t * BQ + 64 * half, a.n, a.P);
           float* p0 = dq_head + tok0 * a.H * D_;
@@ -480,16 +493,24 @@ __global__ void __launch_bounds__(640, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
-  if (a.D != D_) return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(ra_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       BwdCfg::SMEM_BYTES);
+template <int D_>
+cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(ra_bwd_kernel<D_>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       BwdCfg<D_>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.B * a.Hkv * a.P * a.T;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ra_bwd_kernel<<<(unsigned)grid, 640, BwdCfg::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  ra_bwd_kernel<D_><<<(unsigned)grid, 640, BwdCfg<D_>::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
+  if (a.D == 128) return launch_bwd_d<128>(a, tq, tk, tv, tdo, s);
+  if (a.D == 64) return launch_bwd_d<64>(a, tq, tk, tv, tdo, s);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace ra

@@ -204,7 +204,7 @@ ra_status_t ra_shard_work_model(const ra_params_t* p, unsigned long long* host_o
  *   word, fp32 dQ accumulator, D, lse * log2(e)) lives in one 64 MiB array of device
  *   memory inside the library, which every GPU that loads the library holds until the
  *   process exits.  Problems whose ra_bwd_workspace_bytes() exceeds 64 MiB are rejected
- *   with RA_ERR_WORKSPACE (roughly B * L * H above 128K rows at head_dim 128).
+ *   with RA_ERR_WORKSPACE (roughly B * L * H above 128K rows at head_dim 128, 256K at 64).
  *   The first call on a device looks up the array's device address with that device
  *   current (set-up); make that first call before any stream capture.
  *   Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
@@ -349,7 +349,7 @@ typedef struct {
 
 /* Bytes of workspace for a forward followed by a backward (>= ra_bpt_workspace_bytes; the
  * forward's part of the layout is the same), 0 if `p` is invalid or has no backward
- * kernel (head_dim must be 128 and d_model <= 4096). */
+ * kernel (d_model must be at most 4096). */
 size_t ra_bpt_train_workspace_bytes(const ra_bpt_params_t* p);
 
 /*

@@ -86,8 +86,19 @@ def test_bwd_layouts_agree():
         assert float((w.float() - y.float()).norm() / y.float().norm()) <= GRAD_TOL
 
 
-def test_bwd_unsupported_head_dim():
-    q, k, v, do = (t.cuda() for t in make_inputs(1, 512, 1, 64, seed=1))
-    out, lse = era.ra_fwd(q, k, v, 4, 128, "striped", True)
-    with pytest.raises(era.RaError, match="RA_ERR_UNSUPPORTED"):
-        era.ra_bwd(q, k, v, out, lse, do, 4, 128, "striped", True)
+@pytest.mark.parametrize("B,L,H,Hkv,P,block,layout,causal", [
+    (1, 2048, 2, 2, 4, 128, "striped", True),
+    (2, 1536, 3, 3, 4, 128, "contiguous", True),    # 3 KV tiles per shard, batch 2
+    (1, 2048, 4, 2, 4, 256, "zigzag", True),        # grouped-query, 2:1
+    (1, 1024, 2, 1, 1, 128, "contiguous", True),    # P = 1, one KV head
+    (1, 1024, 2, 2, 4, 128, "striped", False),
+])
+def test_bwd_head_dim_64(B, L, H, Hkv, P, block, layout, causal):
+    # head_dim 64: the kernel keeps K 128 features wide (the upper half zero) so that
+    # dQ^T = K^T dS^T is still an M = 128 product; only its first 64 rows are drained
+    q, k, v, do = make_inputs(B, L, H, 64, seed=640 + L + H, kv_heads=Hkv)
+    q64, k64, v64, do64 = to_f64(q, k, v, do)
+    dq_r, dk_r, dv_r = oracle.gqa_bwd(q64, k64, v64, do64, causal)
+    dq, dk, dv = _run(q, k, v, do, P, block, layout, causal)
+    errs = (_rel(dq, dq_r), _rel(dk, dk_r), _rel(dv, dv_r))
+    assert max(errs) <= GRAD_TOL, errs
