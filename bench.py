@@ -7,7 +7,7 @@ causal-useful work only: per unmasked (query, key) pair 4*D forward and 10*D bac
 (five products, the recompute included).
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload 32k|262k|1m|8k|32k-gqa|32k-bpt]
+                  [--workload 32k|262k|1m|8k|32k-gqa|32k-d64|32k-bpt]
                   [--layout striped|contiguous|zigzag] [--impl ours|reference]
 
 N > 1 runs under torchrun: every rank runs an independent replica on its own GPU (the
@@ -40,7 +40,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="32k",
-                    choices=["8k", "32k", "262k", "1m", "32k-gqa", "32k-bpt"])
+                    choices=["8k", "32k", "262k", "1m", "32k-gqa", "32k-d64", "32k-bpt"])
     ap.add_argument("--layout", default=None, choices=["striped", "contiguous", "zigzag"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

@@ -8,7 +8,7 @@ values widened to float64.  This module holds no attention arithmetic.
 
 import torch
 
-# The five workloads of this library's test and benchmark plan.
+# The workloads of this library's test and benchmark plan.
 WORKLOADS = {
     "tiny":  dict(batch=1, heads=2, head_dim=64, seq_len=512, P=4, block=128,
                   causal=False, layouts=("contiguous",), backward=False),
@@ -23,6 +23,9 @@ WORKLOADS = {
     # grouped-query attention: 32 query heads on 8 key/value heads (4 per group)
     "32k-gqa": dict(batch=1, heads=32, kv_heads=8, head_dim=128, seq_len=32768, P=8,
                     block=128, causal=True, layouts=("zigzag", "striped"), backward=True),
+    # head dim 64 at the 32k workload's width: 64 heads of 64
+    "32k-d64": dict(batch=1, heads=64, head_dim=64, seq_len=32768, P=8, block=128,
+                    causal=True, layouts=("zigzag", "striped"), backward=True),
     # one blockwise transformer layer (forward): d_model 4096 = 32 x 128, d_ff = 4 d_model,
     # the feed-forward part in blocks of 16384 rows
     "32k-bpt": dict(batch=1, heads=32, head_dim=128, seq_len=32768, P=8, block=128,
@@ -31,7 +34,7 @@ WORKLOADS = {
 }
 
 SEEDS = {"tiny": 1000, "8k": 1001, "32k": 1002, "262k": 1003, "1m": 1004, "32k-gqa": 1005,
-         "32k-bpt": 1006}
+         "32k-bpt": 1006, "32k-d64": 1007}
 
 
 def make_inputs(batch, seq_len, heads, head_dim, seed, device="cpu", with_dout=True,

@@ -29,7 +29,7 @@ def _rows(L, P, layout):
 
 
 CASES = [("32k", "striped"), ("262k", "striped"), ("1m", "striped"), ("1m", "contiguous"),
-         ("32k", "zigzag"), ("1m", "zigzag"), ("32k-gqa", "zigzag")]
+         ("32k", "zigzag"), ("1m", "zigzag"), ("32k-gqa", "zigzag"), ("32k-d64", "zigzag")]
 
 
 @pytest.mark.parametrize("name,layout", CASES)
