@@ -375,16 +375,27 @@ def run_ours(args, w, rank, world, local):
     # step s-1's results come down) on copy streams while step s computes.
     e2e = None
     if not args.no_e2e:
-        hin = [t.cpu().pin_memory() for t in (q, k, v, do)]
+        # host side: one pinned allocation holding the inputs and one set of results (every
+        # step's results land there in turn).  Separate pinned buffers per tensor and per
+        # set stalled the copies for tens of ms now and then on a virtualised host.
+        ins, outs = [q, k, v, do], [out, lse, dq, dk, dv]
+        blob = torch.empty(sum(t.numel() * t.element_size() for t in ins + outs),
+                           dtype=torch.uint8, pin_memory=True)
+        views, off = [], 0
+        for t in ins + outs:
+            nb = t.numel() * t.element_size()
+            views.append(blob[off:off + nb].view(t.dtype).view(t.shape))
+            off += nb
+        hin, hout_shared = views[:4], views[4:]
+        for h_, t in zip(hin, ins):
+            h_.copy_(t.cpu())
         h2d = sum(t.numel() * t.element_size() for t in hin)
         sets = []
         for bset in range(2):
-            din = [q, k, v, do] if bset == 0 else [torch.empty_like(t) for t in (q, k, v, do)]
-            dout = ([out, lse, dq, dk, dv] if bset == 0 else
-                    [torch.empty_like(t) for t in (out, lse, dq, dk, dv)])
-            hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dout]
+            din = ins if bset == 0 else [torch.empty_like(t) for t in ins]
+            dout = outs if bset == 0 else [torch.empty_like(t) for t in outs]
             ev = {n: torch.cuda.Event() for n in ("up", "done", "down")}
-            sets.append((din, dout, hout, ev))
+            sets.append((din, dout, hout_shared, ev))
         d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
         s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
