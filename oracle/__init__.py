@@ -39,18 +39,19 @@ finite differences, the pages' printed demo output).  None is "parity unpinned".
 """
 
 from .attention import (attention_fwd, attention_bwd, attention_rows_fwd, attention_rows_dq,
-                        brute_force_fwd, default_scale)
+                        attention_cols_dkdv, brute_force_fwd, default_scale)
 from .ring import ring_fwd, ring_partials, merge_partials
 from .work import (shard_of, local_of, shard_tokens, ring_order, shard_work,
                    tile_class)
-from .gqa import gqa_fwd, gqa_bwd, group_size
+from .gqa import gqa_fwd, gqa_bwd, gqa_cols_dkdv, group_size
 from .bpt import (bpt_layer_bwd, bpt_layer_fwd, bpt_layer_fwd_blocked, bpt_layer_rows, gelu,
                   gelu_grad, layer_norm, layer_norm_bwd)
 
 __all__ = [
-    "attention_fwd", "attention_bwd", "attention_rows_fwd", "attention_rows_dq", "brute_force_fwd",
+    "attention_fwd", "attention_bwd", "attention_rows_fwd", "attention_rows_dq",
+    "attention_cols_dkdv", "brute_force_fwd",
     "default_scale", "ring_fwd", "ring_partials", "merge_partials", "shard_of",
-    "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class", "gqa_fwd", "gqa_bwd",
+    "local_of", "shard_tokens", "ring_order", "shard_work", "tile_class", "gqa_fwd", "gqa_bwd", "gqa_cols_dkdv",
     "group_size", "bpt_layer_fwd", "bpt_layer_fwd_blocked", "bpt_layer_rows", "bpt_layer_bwd",
     "gelu", "gelu_grad", "layer_norm", "layer_norm_bwd",
 ]

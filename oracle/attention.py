@@ -32,10 +32,14 @@ lse is [B, H, L].
 """
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
 _ROW_BLOCK = 256
+# attention_cols_dkdv: values in one block's score matrix (bounds its memory)
+_COL_BLOCK_VALUES = 1 << 26
 
 
 def default_scale(head_dim):
@@ -63,15 +67,20 @@ def _scores(Qr, K, r0, causal, scale):
 
 
 def _softmax_rows(s):
-    """Exact two-pass softmax over full rows: returns (p, lse)."""
+    """Exact two-pass softmax over full rows: returns (p, lse).
+
+    A row with no visible key (every score -inf) gets p = 0 and lse = -inf.  Only that
+    case is guarded: a NaN score (from a NaN input) makes its whole row's p and lse NaN,
+    as the arithmetic gives."""
     m = np.max(s, axis=1, keepdims=True)
     finite = np.isfinite(m)
     m_safe = np.where(finite, m, 0.0)
-    e = np.exp(s - m_safe)
+    with np.errstate(invalid="ignore"):
+        e = np.exp(s - m_safe)
     tot = np.sum(e, axis=1, keepdims=True)
     with np.errstate(divide="ignore", invalid="ignore"):
-        lse = np.where(tot > 0, m_safe + np.log(tot), -np.inf)
-        p = np.where(tot > 0, e / tot, 0.0)
+        lse = np.where(tot == 0, -np.inf, m_safe + np.log(tot))
+        p = np.where(tot == 0, 0.0, e / tot)
     return p, lse[:, 0]
 
 
@@ -139,6 +148,64 @@ def attention_rows_dq(q, k, v, dout, b, h, rows, causal, scale=None):
         gq, _, _ = _grad_rows(p, Qr, K, V, dOr, scale)
         out[n] = gq[0]
     return out
+
+
+def attention_cols_dkdv(q, k, v, dout, b, h, cols, causal, scale=None, threads=None):
+    """dK and dV for a few sampled key columns of one (batch, head).
+
+    Used where the full backward is too large for the CPU.  By the formulas in the module
+    docstring, key column c collects one term from every query row r that sees it (r >= c
+    when causal, every row otherwise):
+        dK_c = sum_r dS[r, c] q_r ,   dV_c = sum_r p[r, c] dO_r ,
+    and each such row needs its own whole softmax row (p[r, c] = exp(s[r, c] - lse_r)) and
+    its output O_r (for D_r = dO_r . O_r).  The cost is O(R * L * D) for the R rows that see
+    the earliest sampled column, so the last columns of a long sequence are cheap.
+
+    The rows are taken in independent blocks (each block's terms are computed on its own
+    thread: NumPy releases the interpreter lock inside its array operations); the blocks'
+    terms are then added in row order.  Returns (dk [len(cols), D], dv [len(cols), D]).
+    """
+    L, D = q.shape[1], q.shape[3]
+    if scale is None:
+        scale = default_scale(D)
+    cols = np.asarray(cols, dtype=np.int64)
+    K = np.asarray(k[b, :, h, :], dtype=np.float64)
+    V = np.asarray(v[b, :, h, :], dtype=np.float64)
+    Kc, Vc = K[cols], V[cols]
+    r_first = int(cols.min()) if causal else 0
+    step = max(1, _COL_BLOCK_VALUES // L)         # rows per block
+
+    def block_terms(r0):
+        r1 = min(L, r0 + step)
+        C = r1 if causal else L
+        Qr = np.asarray(q[b, r0:r1, h, :], dtype=np.float64)
+        dOr = np.asarray(dout[b, r0:r1, h, :], dtype=np.float64)
+        s = scale * (Qr @ K[:C].T)
+        if causal:      # c > r happens only among the block's own keys [r0, r1)
+            own = s[:, r0:C]
+            own[np.triu_indices(r1 - r0, 1)] = -np.inf
+        p, _ = _softmax_rows(s)
+        Dr = np.sum(dOr * (p @ V[:C]), axis=1, keepdims=True)
+        # p at the sampled columns; a column at or past C is masked for every row here
+        pc = np.zeros((r1 - r0, len(cols)))
+        seen = cols < C
+        pc[:, seen] = p[:, cols[seen]]
+        dSc = pc * (dOr @ Vc.T - Dr) * scale
+        return dSc.T @ Qr, pc.T @ dOr
+
+    starts = list(range(r_first, L, step))
+    n_thr = threads or min(len(starts), len(os.sched_getaffinity(0)), 4)
+    if n_thr > 1:
+        with ThreadPoolExecutor(max_workers=n_thr) as ex:
+            parts = list(ex.map(block_terms, starts))
+    else:
+        parts = [block_terms(r0) for r0 in starts]
+    dk = np.zeros((len(cols), D))
+    dv = np.zeros((len(cols), D))
+    for gk, gv in parts:
+        dk += gk
+        dv += gv
+    return dk, dv
 
 
 def attention_bwd(q, k, v, dout, causal, scale=None):

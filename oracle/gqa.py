@@ -24,7 +24,7 @@ per-query-head dK, dV are summed over each group.
 
 import numpy as np
 
-from .attention import attention_bwd, attention_fwd
+from .attention import attention_bwd, attention_cols_dkdv, attention_fwd
 
 
 def group_size(q_heads, kv_heads):
@@ -49,3 +49,17 @@ def gqa_bwd(q, k, v, dout, causal, scale=None):
     dq, dk_e, dv_e = attention_bwd(q, _expand(k, G), _expand(v, G), dout, causal, scale)
     B, L, Hkv, D = k.shape
     return dq, dk_e.reshape(B, L, Hkv, G, D).sum(3), dv_e.reshape(B, L, Hkv, G, D).sum(3)
+
+
+def gqa_cols_dkdv(q, k, v, dout, b, hk, cols, causal, scale=None):
+    """dK and dV of key/value head hk at a few sampled key columns: the sum, over the G
+    query heads h = hk * G + g that read that head, of each query head's column terms
+    (``attention_cols_dkdv``).  Returns (dk [len(cols), D], dv [len(cols), D])."""
+    G = group_size(q.shape[2], k.shape[2])
+    dk = dv = 0.0
+    for g in range(G):
+        h = hk * G + g
+        gk, gv = attention_cols_dkdv(q[:, :, h:h + 1], k[:, :, hk:hk + 1], v[:, :, hk:hk + 1],
+                                     dout[:, :, h:h + 1], b, 0, cols, causal, scale)
+        dk, dv = dk + gk, dv + gv
+    return dk, dv

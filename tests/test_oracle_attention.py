@@ -126,6 +126,50 @@ def test_rows_dq_matches_full_backward():
         assert np.max(np.abs(got - dq[0, rows, 1, :])) < 1e-13
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_cols_dkdv_matches_full_backward(causal, monkeypatch):
+    q, k, v, dout = _rand(1, 150, 2, 8, seed=15)
+    _, dk, dv = oracle.attention_bwd(q, k, v, dout, causal)
+    cols = [0, 7, 64, 148, 149]
+    # several row blocks of a few rows each (the block size only bounds memory)
+    for budget in (oatt._COL_BLOCK_VALUES, 6 * 150 + 5):
+        monkeypatch.setattr(oatt, "_COL_BLOCK_VALUES", budget)
+        gk, gv = oracle.attention_cols_dkdv(q, k, v, dout, 0, 1, cols, causal)
+        assert np.max(np.abs(gk - dk[0, cols, 1, :])) < 1e-13
+        assert np.max(np.abs(gv - dv[0, cols, 1, :])) < 1e-13
+
+
+def test_cols_dkdv_matches_library_autograd():
+    """The sampled key columns against torch's library attention and its autograd."""
+    q, k, v, dout = _rand(1, 90, 2, 16, seed=16)
+    tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(x.transpose(0, 2, 1, 3))).requires_grad_()
+                  for x in (q, k, v))
+    o = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+    o.backward(torch.from_numpy(np.ascontiguousarray(dout.transpose(0, 2, 1, 3))))
+    cols = [3, 45, 80, 89]
+    for h in range(2):
+        gk, gv = oracle.attention_cols_dkdv(q, k, v, dout, 0, h, cols, causal=True)
+        assert np.max(np.abs(gk - tk.grad.numpy()[0, h, cols, :])) < 1e-12
+        assert np.max(np.abs(gv - tv.grad.numpy()[0, h, cols, :])) < 1e-12
+
+
+def test_planted_unmasked_late_column_is_caught():
+    """A column after a row's position must get nothing from that row: summing the
+    unmasked terms instead fails the library pin."""
+    q, k, v, dout = _rand(1, 40, 1, 8, seed=17)
+    tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(x.transpose(0, 2, 1, 3))).requires_grad_()
+                  for x in (q, k, v))
+    o = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+    o.backward(torch.from_numpy(np.ascontiguousarray(dout.transpose(0, 2, 1, 3))))
+    cols = [10, 30]
+    right = oracle.attention_cols_dkdv(q, k, v, dout, 0, 0, cols, causal=True)
+    # the non-causal column terms on causal probabilities would be the plausible slip
+    wrong = oracle.attention_cols_dkdv(q, k, v, dout, 0, 0, cols, causal=False)
+    want = tv.grad.numpy()[0, 0, cols, :]
+    assert np.max(np.abs(right[1] - want)) < 1e-12
+    assert np.max(np.abs(wrong[1] - want)) > 1e-3
+
+
 def _loss(q, k, v, dout, causal):
     out, _ = oracle.attention_fwd(q, k, v, causal)
     return float(np.sum(out * dout))

@@ -102,3 +102,17 @@ def test_planted_mistakes_fail_the_library_pin():
     _, dk_e, _ = oracle.attention_bwd(q, np.repeat(k, 2, axis=2), np.repeat(v, 2, axis=2), do,
                                       True)
     assert np.max(np.abs(dk_e[:, :, ::2] - dk_ref)) > 1e-2
+
+
+@pytest.mark.parametrize("shape", [(1, 37, 4, 2, 8), (1, 64, 3, 1, 16)])
+def test_gqa_cols_dkdv_matches_library(shape):
+    """The sampled key columns of each shared head against the library's grouped-query
+    autograd (the sum over the group included)."""
+    q, k, v, do = _rand(*shape, seed=31)
+    _, _, gk, gv = _sdpa_gqa(q, k, v, do, True)
+    L, Hkv = shape[1], shape[3]
+    cols = [0, L // 2, L - 1]
+    for hk in range(Hkv):
+        dk, dv = oracle.gqa_cols_dkdv(q, k, v, do, 0, hk, cols, causal=True)
+        assert np.max(np.abs(dk - gk[0, cols, hk])) < 1e-12
+        assert np.max(np.abs(dv - gv[0, cols, hk])) < 1e-12
