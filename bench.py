@@ -7,8 +7,11 @@ causal-useful work only: per unmasked (query, key) pair 4*D forward and 10*D bac
 (five products, the recompute included).
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload 32k|262k|1m|8k|32k-gqa|32k-d64|32k-bpt]
+                  [--workload 1m|262k|32k|8k|32k-gqa|32k-d64|32k-bpt]
                   [--layout striped|contiguous|zigzag] [--impl ours|reference]
+
+The default workload is the largest one: 1,048,576 tokens, 8 heads of 128, P = 32 virtual
+shards, block 256, causal, striped.
 
 N > 1 runs under torchrun: every rank runs an independent replica on its own GPU (the
 path has no exchange between GPUs); the rate is all ranks' FLOPs over the slowest
@@ -36,10 +39,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 4 for the 1M-token workload, else 10)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="32k",
+    ap.add_argument("--workload", default="1m",
                     choices=["8k", "32k", "262k", "1m", "32k-gqa", "32k-d64", "32k-bpt"])
     ap.add_argument("--layout", default=None, choices=["striped", "contiguous", "zigzag"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -47,18 +51,41 @@ def parse_args():
     ap.add_argument("--no-merge", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="layer workload only: forward + backward of the layer per step")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload with this many heads (a smaller case of the same "
+                         "kernels, e.g. for a profiler capture)")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
+    if a.steps is None:
+        a.steps = 4 if a.workload == "1m" else 10
     return a
 
 
-def workload(name, layout):
+def workload(name, layout, heads=None):
     from exact_blockwise_ring_gb300.synthetic import WORKLOADS, SEEDS
     w = dict(WORKLOADS[name])
     w["name"] = name
     w["seed"] = SEEDS[name]
     w["layout"] = layout or w["layouts"][0]
+    if heads is not None and heads != w["heads"]:
+        # fewer (or more) heads of the same shape: grouped-query workloads keep their
+        # group size
+        g = w["heads"] // w.get("kv_heads", w["heads"])
+        if heads % g:
+            raise SystemExit("--heads must be a multiple of the group size %d" % g)
+        w["heads"] = heads
+        if "kv_heads" in w:
+            w["kv_heads"] = heads // g
+        w["name"] = "%s-h%d" % (name, heads)
     return w
+
+
+def workload_key(w):
+    """The shape a traffic capture belongs to (heads excluded: heads are independent
+    problems run one after another, so DRAM traffic scales with their number)."""
+    return "L%d-g%d-D%d-P%d-b%d-%s%s" % (
+        w["seq_len"], w["heads"] // w.get("kv_heads", w["heads"]), w["head_dim"], w["P"],
+        w["block"], w["layout"], "" if w["causal"] else "-noncausal")
 
 
 def pairs_of(L, causal):
@@ -244,18 +271,32 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel, src_files):
-    """DRAM bytes per launch from the committed ncu summary (profiles/ncu_traffic.txt), if
-    the kernel source has not changed since it was captured; else None."""
+def traffic_for(kernel, src_files, w):
+    """DRAM bytes per launch of `kernel` on workload `w`, from the committed ncu summary
+    (profiles/ncu_traffic.txt): a capture of the same shape (workload_key) with the same
+    kernel source, taken with H_c heads, scaled by H / H_c (heads are independent and run
+    one after another).  Returns (bytes, note) or (None, reason)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
-        return None
+        return None, "no capture"
+    key, heads, h = workload_key(w), w["batch"] * w["heads"], source_hash(*src_files)
+    stale = False
     with open(p) as f:
         for ln in f:
             fl = ln.split()
-            if len(fl) >= 5 and not ln.startswith("#") and fl[0] == kernel:
-                return int(fl[1]) if fl[4] == source_hash(*src_files) else None
-    return None
+            if len(fl) < 7 or ln.startswith("#") or fl[0] != kernel or fl[5] != key:
+                continue
+            if fl[4] != h:
+                stale = True
+                continue
+            cap_heads = int(fl[6])
+            scaled = int(fl[1]) * heads // cap_heads
+            if cap_heads == heads:
+                return scaled, "captured on this workload"
+            return scaled, "scaled x%g from a capture with %d of the %d heads" % (
+                heads / cap_heads, cap_heads, heads)
+    return None, ("kernel source changed since the capture" if stale
+                  else "no capture of this workload")
 
 
 def hbm_line(nbytes, ms, peak_gbs):
@@ -364,10 +405,20 @@ def run_ours(args, w, rank, world, local):
     else:
         dom, dom_ms, dom_flops, files = "ra_fwd_kernel", fwd_ms, f_fwd, ("ra_fwd.cu",) + hdrs
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    # the burst peak for a step shorter than a second, the sustained one (a seconds-long
+    # loop under the power cap) for longer steps
+    if ms_per_step < 1000.0:
+        peak_use, peak_name = peak_tf, "bf16_tflops (burst: timed step under 1 s)"
+    else:
+        peak_use, peak_name = peak_sus, "bf16_tflops_sustained (timed step of 1 s or more)"
+    traffic, traffic_note = traffic_for(dom, files, w)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
-                "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
-                "peak_kind": "bf16_tflops_sustained of %s" % pk_kind,
-                "traffic": traffic_for(dom, files)}
+                "peak": peak_use, "unit": "TFLOP/s", "frac": round(achieved / peak_use, 4),
+                "peak_kind": "%s of %s" % (peak_name, pk_kind),
+                "frac_of_burst": round(achieved / peak_tf, 4),
+                "frac_of_sustained": round(achieved / peak_sus, 4),
+                "flops_per_launch": dom_flops, "ms_per_launch": round(dom_ms, 3),
+                "traffic": traffic, "traffic_note": traffic_note}
 
     # end to end through the public API with host buffers: every step copies its inputs
     # from pinned host memory, makes the two calls, and copies every result back.  Steps
@@ -426,16 +477,18 @@ def run_ours(args, w, rank, world, local):
         for sidx in range(2):
             e2e_step(sidx)
         torch.cuda.synchronize()
-        # three timed windows of K steps each; the line reports the median window and lists
-        # all three (on a virtualised host a single host-memory copy can stall for ~100 ms,
-        # which one window of K steps cannot absorb)
+        # three timed windows of Ke steps each (Ke = K, or fewer when K steps take over
+        # 10 s: seconds-long steps hide their copies anyway); the line reports the median
+        # window and lists all three (on a virtualised host a single host-memory copy can
+        # stall for ~100 ms, which one window cannot absorb)
+        Ke = K if ms_per_step * K <= 10000.0 else max(1, int(10000.0 // ms_per_step))
         windows = []
         for _ in range(3):
             dist_barrier(world)
             a0 = torch.cuda.Event(enable_timing=True)
             a1 = torch.cuda.Event(enable_timing=True)
             a0.record(s_up)
-            for sidx in range(K):
+            for sidx in range(Ke):
                 e2e_step(sidx)
             s_down.wait_stream(stream)
             a1.record(s_down)
@@ -459,14 +512,14 @@ def run_ours(args, w, rank, world, local):
                 c1.record(s_)
             torch.cuda.synchronize()
             link[name] = round(nb / (c0.elapsed_time(c1) * 1e-3) / 1e9, 1)
-        e2e = {"value": round(job_rate(world, step_flops, K, e_ms), 2),
+        e2e = {"value": round(job_rate(world, step_flops, Ke, e_ms), 2),
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e_ms / K, 3),
-               "windows": [round(job_rate(world, step_flops, K, x), 2) for x in windows],
+               "ms_per_step": round(e_ms / Ke, 3), "steps_per_window": Ke,
+               "windows": [round(job_rate(world, step_flops, Ke, x), 2) for x in windows],
                "host_link": link,
                "copies": "each step's H2D and D2H overlap the neighbouring steps' compute "
                          "(two buffer sets, two copy streams); value = the median of three "
-                         "timed windows of K steps (all three in windows)"}
+                         "timed windows of steps_per_window steps (all three in windows)"}
 
     # the bandwidth-bound kernels against the measured HBM copy rate: the backward's
     # preprocess and finalize (timed inside the steps above) and the partial merge (timed
@@ -512,6 +565,17 @@ def run_ours(args, w, rank, world, local):
                                    for n, u in enumerate(("tiles", "pairs", "visits"))}
     balance["unit"] = "max / mean over the P shards"
 
+    # the step's time scaled to the maximum SM clock (time x median clock / max clock):
+    # compares layouts or runs whose clocks differed (the power cap), assuming the
+    # tensor-bound kernels scale with the SM clock
+    clock_norm = None
+    if clk and clk.get("sm_mhz") and clk.get("sm_max_mhz"):
+        f = clk["sm_mhz"] / clk["sm_max_mhz"]
+        clock_norm = {"ms_per_step": round(ms_per_step * f, 3),
+                      "fwd_ms": round(fwd_ms * f, 3), "bwd_main_ms": round(main_ms * f, 3),
+                      "value": round(value / f, 2),
+                      "rule": "time x median SM MHz / max SM MHz over the timed region"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
@@ -529,7 +593,8 @@ def run_ours(args, w, rank, world, local):
                 "cpu_baseline": cpu,
                 "e2e": e2e,
                 "tflops_12d": round(value * 12.0 / 14.0, 2),
-                "mufu": mufu, "gpu_launches": 4 * K, "clocks": clk}
+                "mufu": mufu, "gpu_launches": 4 * K, "clocks": clk,
+                "at_max_clock": clock_norm}
         print(json.dumps(line), flush=True)
 
 
@@ -732,7 +797,7 @@ def run_reference(args, w, rank, world):
 
 def main():
     args = parse_args()
-    w = workload(args.workload, args.layout)
+    w = workload(args.workload, args.layout, args.heads)
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores; other ranks exit without work
         run_reference(args, w, int(os.environ.get("RANK", "0")),

@@ -65,12 +65,22 @@ __global__ void __launch_bounds__(256)
       }
       lv[g] = g < n_parts ? __ldg(lse_parts + g * part_l + r) : kNegInf;
     }
+    // fmaxf skips NaN operands, so a NaN lse (a part whose rows met a NaN input) is
+    // noted separately and makes the row's output and lse NaN
     float mx = kNegInf;
+    bool nan = false;
 #pragma unroll
-    for (int g = 0; g < kPrefetch; ++g) mx = fmaxf(mx, lv[g]);
-    for (int g = kPrefetch; g < n_parts; ++g) mx = fmaxf(mx, __ldg(lse_parts + g * part_l + r));
-    float tot = 0.f;
-    if (mx != kNegInf) {
+    for (int g = 0; g < kPrefetch; ++g) {
+      mx = fmaxf(mx, lv[g]);
+      nan |= lv[g] != lv[g];
+    }
+    for (int g = kPrefetch; g < n_parts; ++g) {
+      const float l = __ldg(lse_parts + g * part_l + r);
+      mx = fmaxf(mx, l);
+      nan |= l != l;
+    }
+    float tot = nan ? __int_as_float(0x7fc00000) : 0.f;
+    if (!nan && mx != kNegInf) {
 #pragma unroll
       for (int g = 0; g < kPrefetch; ++g)
         if (lv[g] != kNegInf) tot += expf(lv[g] - mx);
@@ -81,8 +91,9 @@ __global__ void __launch_bounds__(256)
     }
     const float inv = tot > 0.f ? 1.f / tot : 0.f;
     if (act) {
-      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+      float4 a0 = make_float4(tot, tot, tot, tot), a1 = a0;   // NaN rows stay NaN
       if (tot > 0.f) {
+        a0 = a1 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int g = 0; g < kPrefetch; ++g) {
           if (lv[g] == kNegInf) continue;   // skipped (or absent), whatever its partial holds
@@ -103,7 +114,7 @@ __global__ void __launch_bounds__(256)
       store4(out, out_fp32, e, a0);
       store4(out, out_fp32, e + 4, a1);
     }
-    if (sub == 0) lse[r] = tot > 0.f ? mx + logf(tot) : kNegInf;
+    if (sub == 0) lse[r] = tot > 0.f ? mx + logf(tot) : (nan ? tot : kNegInf);
   }
 }
 
@@ -223,18 +234,17 @@ cudaError_t launch_merge(int n_parts, const float* o_parts, const float* lse_par
   const long long rows = (long long)B * L * H;
   int lpr = 1;
   while (lpr < D / 8) lpr <<= 1;
-  // as many blocks as are resident at once (every SM full), striding over the rows
-  static int cap = 0;
-  if (cap == 0) {
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_kernel, 256, 0) != cudaSuccess)
-      return cudaGetLastError();
-    cap = sms * (per_sm > 0 ? per_sm : 1);
-  }
+  // as many blocks as are resident at once on the current device (every SM full),
+  // striding over the rows; looked up on every call (a few microseconds of host work)
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_kernel, 256, 0);
+  if (e != cudaSuccess) return e;
+  const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
   unsigned grid = grid_for(rows, 256 / lpr);
-  if (grid > (unsigned)cap) grid = (unsigned)cap;
+  if ((long long)grid > cap) grid = (unsigned)cap;
   merge_kernel<<<grid, 256, 0, s>>>(n_parts, o_parts, lse_parts, B, L, H, D, lpr, out, out_fp32,
                                     lse);
   return cudaGetLastError();

@@ -444,9 +444,10 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const int loc = t * kTile + arow;
       const long long tok = token_of(a.layout, i, loc, a.n, a.P);
+      // l = 0: no visible key (out 0, lse -inf); a NaN row sum (a NaN input) stays NaN
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_v =
-          l_run > 0.f ? (m_run * sl2 + __log2f(l_run)) * 0.69314718055994531f : kNegInf;
+          l_run == 0.f ? kNegInf : (m_run * sl2 + __log2f(l_run)) * 0.69314718055994531f;
       const size_t row = ((size_t)b * a.L + tok) * a.H + h;
       const size_t lidx = ((size_t)b * a.H + h) * a.L + tok;
       float* of32 = nullptr;

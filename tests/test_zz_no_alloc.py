@@ -5,7 +5,7 @@ allocator, or a latency-critical path that may not call cudaMalloc because it ca
 the device) has no workspace to pass; the entry point uses scratch memory built into the
 library instead.  These tests call it through the C ABI and compare it with ra_bwd on the
 same inputs, twice in a row, because the built-in scratch keeps the previous call's
-contents.  This file is collected last on purpose.
+contents, and once with the fp64 oracle.  This file is collected last on purpose.
 """
 
 import ctypes
@@ -14,9 +14,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import exact_blockwise_ring_gb300 as era
 from exact_blockwise_ring_gb300 import api
-from exact_blockwise_ring_gb300.synthetic import make_inputs
+from exact_blockwise_ring_gb300.synthetic import make_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +58,14 @@ def test_noalloc_backward_matches_workspace_backward_twice(layout, Hkv):
         for got, want, name in zip((dq, dk, dv), ref, ("dq", "dk", "dv")):
             assert torch.isfinite(got).all(), (call, name)
             assert _rel(got, want) <= GRAD_TOL, (call, name, _rel(got, want))
+        # dK and dV are accumulated on chip in a fixed order: the same bits as ra_bwd's
+        # (dQ's fp32 reductions land in any order, so it is held to the tolerance above)
+        assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2]), call
+    # and against the fp64 oracle (grouped-query backward on the same bf16 inputs)
+    g_ref = oracle.gqa_bwd(*to_f64(q, k, v, do), causal=True)
+    for got, want, name in zip((dq, dk, dv), g_ref, ("dq", "dk", "dv")):
+        e = float(np.linalg.norm(got.double().cpu().numpy() - want) / np.linalg.norm(want))
+        assert e <= GRAD_TOL, (name, e)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
