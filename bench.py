@@ -399,7 +399,7 @@ def run_ours(args, w, rank, world, local):
     peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
 
     # dominant kernel and its roofline (tensor-bound contraction)
-    hdrs = ("ra_internal.h", "ra_ptx.cuh", "ra_rows.cuh")     # included by both kernels
+    hdrs = ("ra_internal.h", "ra_ptx.cuh", "ra_rows.cuh", "ra_exp2.cuh")   # shared headers
     if main_ms >= fwd_ms:
         dom, dom_ms, dom_flops, files = "ra_bwd_kernel", main_ms, f_bwd, ("ra_bwd.cu",) + hdrs
     else:

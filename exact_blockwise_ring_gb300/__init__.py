@@ -9,11 +9,12 @@ from .api import (BPT_WEIGHTS, LAYOUTS, BptGrads, BptLayer, BptParams, BptWeight
                   RaError, RingAttention, Workspace, bpt_train_workspace_bytes,
                   bpt_workspace_bytes, bwd_workspace_bytes, fwd_workspace_bytes,
                   header_symbols, lib, make_bpt_params, make_params, ra_bpt_bwd, ra_bpt_fwd, ra_bwd,
-                  ra_bwd_stages, ra_fwd, ra_layernorm, ra_linear, ra_merge, ra_selftest_timeout,
+                  ra_bwd_stages, ra_fwd, ra_layernorm, ra_linear, ra_merge, ra_selftest_exp2,
+                  ra_selftest_timeout,
                   ra_shard_work_model, ring_attention)
 
 __all__ = ["BPT_WEIGHTS", "LAYOUTS", "BptGrads", "BptLayer", "BptParams", "BptWeights", "Params",
            "RaError", "RingAttention", "Workspace", "bpt_train_workspace_bytes",
            "bpt_workspace_bytes", "bwd_workspace_bytes", "fwd_workspace_bytes", "header_symbols",
            "lib", "make_bpt_params", "make_params", "ra_bpt_bwd", "ra_bpt_fwd", "ra_bwd", "ra_bwd_stages", "ra_fwd", "ra_layernorm", "ra_linear",
-           "ra_merge", "ra_selftest_timeout", "ra_shard_work_model", "ring_attention"]
+           "ra_merge", "ra_selftest_exp2", "ra_selftest_timeout", "ra_shard_work_model", "ring_attention"]

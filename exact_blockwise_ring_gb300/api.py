@@ -13,12 +13,13 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libra.so")
+# RA_LIBRARY selects another build of the library (e.g. the checked build libra_checked.so)
+LIB_PATH = os.environ.get("RA_LIBRARY") or os.path.join(_HERE, "libra.so")
 HEADER_PATH = os.path.join(_HERE, "..", "include", "ra.h")
 
 LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
 STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_WORKSPACE",
-          4: "RA_ERR_CUDA", 5: "RA_ERR_DEVICE_TIMEOUT"}
+          4: "RA_ERR_CUDA", 5: "RA_ERR_DEVICE_TIMEOUT", 6: "RA_ERR_CHECK"}
 RA_BF16, RA_FP32 = 0, 1
 
 
@@ -94,6 +95,8 @@ _SIGS = {
     "ra_bpt_bwd": (ctypes.c_int, [ctypes.POINTER(BptParams), _P, ctypes.POINTER(BptWeights), _P,
                                   ctypes.POINTER(BptGrads), _P, ctypes.c_size_t, _P]),
     "ra_last_error_message": (ctypes.c_char_p, []),
+    "ra_selftest_exp2": (ctypes.c_int, [_P, _P, _P, ctypes.c_longlong, _P]),
+    "ra_checks_enabled": (ctypes.c_int, []),
 }
 
 
@@ -284,6 +287,14 @@ def ra_shard_work_model(seq_len, P, block, layout, causal):
     _check(lib().ra_shard_work_model(ctypes.byref(prm), arr))
     vals = list(arr)
     return {"tiles": vals[:P], "pairs": vals[P:2 * P], "visits": vals[2 * P:]}
+
+
+def ra_selftest_exp2(x, stream=None):
+    """Both 2^x forms of the softmax kernels on a CUDA fp32 tensor: (software, hardware)."""
+    _want(x, torch.float32, "x")
+    y_soft, y_hw = torch.empty_like(x), torch.empty_like(x)
+    _check(lib().ra_selftest_exp2(_ptr(x), _ptr(y_soft), _ptr(y_hw), x.numel(), _stream(stream)))
+    return y_soft, y_hw
 
 
 def ra_selftest_timeout(workspace, timeout_us, stream=None):

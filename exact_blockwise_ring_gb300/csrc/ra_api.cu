@@ -6,6 +6,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "ra_check.cuh"
 #include "ra_internal.h"
 #include "ra_layer.h"
 
@@ -250,6 +251,7 @@ const char* ra_status_string(ra_status_t s) {
     case RA_ERR_WORKSPACE: return "RA_ERR_WORKSPACE";
     case RA_ERR_CUDA: return "RA_ERR_CUDA";
     case RA_ERR_DEVICE_TIMEOUT: return "RA_ERR_DEVICE_TIMEOUT";
+    case RA_ERR_CHECK: return "RA_ERR_CHECK";
   }
   return "RA_ERR_UNKNOWN";
 }
@@ -497,6 +499,10 @@ ra_status_t ra_check_error(void* workspace, void* stream) {
     if (word & 0x10u)
       return fail(RA_ERR_CUDA, "the backward kernel found its shared-memory base not 1024-byte "
                   "aligned and did nothing (error word 0x%x)", word);
+    if (word & kChkMask)
+      return fail(RA_ERR_CHECK, "a range check of the checked build failed (error word 0x%x: "
+                  "0x100 TMA box, 0x200 TMEM, 0x400 shared memory, 0x800 global index, "
+                  "0x1000 item count)", word);
     return fail(RA_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%x)", word);
   }
   return RA_OK;
@@ -511,6 +517,18 @@ ra_status_t ra_selftest_timeout(void* workspace, size_t workspace_bytes, unsigne
   cudaError_t e = launch_selftest_timeout(static_cast<unsigned int*>(workspace),
                                           (uint64_t)timeout_us * 1000ull,
                                           reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test kernel launch");
+  return RA_OK;
+}
+
+int ra_checks_enabled(void) { return kChecked ? 1 : 0; }
+
+ra_status_t ra_selftest_exp2(const float* x, float* y_soft, float* y_hw, long long n,
+                             void* stream) {
+  if (!x || !y_soft || !y_hw) return fail(RA_ERR_INVALID_ARG, "null pointer");
+  if (n < 1 || n >= (1LL << 31)) return fail(RA_ERR_INVALID_ARG, "n must be in [1, 2^31)");
+  cudaError_t e =
+      launch_selftest_exp2(x, y_soft, y_hw, n, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "self-test kernel launch");
   return RA_OK;
 }

@@ -2,10 +2,11 @@
 //   * merge of normalised partials (O_g, lse_g) into (O, lse);
 //   * backward preprocess D = rowsum(dO * O) (labhub, section "逆伝播での KV 再循環");
 //   * fp32 dQ accumulator -> bf16 dQ with the softmax scale folded in;
-//   * the bounded-wait self-test kernel.
+//   * the bounded-wait self-test kernel and the 2^x self-test kernel.
 // All of them stream rows of D contiguous elements with 16-byte vector accesses.
 #include <cuda_bf16.h>
 
+#include "ra_exp2.cuh"
 #include "ra_internal.h"
 #include "ra_ptx.cuh"
 
@@ -220,6 +221,22 @@ __global__ void selftest_timeout_kernel(unsigned int* err, uint64_t limit_ns) {
   __syncthreads();
 }
 
+// Both 2^x forms of the softmax kernels on the same inputs (a pair per thread).
+__global__ void selftest_exp2_kernel(const float* __restrict__ x, float* __restrict__ y_soft,
+                                     float* __restrict__ y_hw, long long n) {
+  const long long i = 2 * ((long long)blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x0 = x[i], x1 = i + 1 < n ? x[i + 1] : 0.f;
+  float s0, s1;
+  f2_unpack(exp2_soft_x2(x0, x1), s0, s1);
+  y_soft[i] = s0;
+  y_hw[i] = ex2_approx(x0);
+  if (i + 1 < n) {
+    y_soft[i + 1] = s1;
+    y_hw[i + 1] = ex2_approx(x1);
+  }
+}
+
 unsigned grid_for(long long rows, int rows_per_block) {
   long long g = (rows + rows_per_block - 1) / rows_per_block;
   return (unsigned)(g < 1 ? 1 : g);
@@ -269,6 +286,12 @@ cudaError_t launch_dq_convert(const float* dq_acc, void* dq, float scale, size_t
   if (blocks < 1) blocks = 1;
   dq_convert_kernel<<<(unsigned)blocks, 256, 0, s>>>(
       dq_acc, reinterpret_cast<__nv_bfloat16*>(dq), scale, n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_exp2(const float* x, float* y_soft, float* y_hw, long long n,
+                                 cudaStream_t s) {
+  selftest_exp2_kernel<<<grid_for((n + 1) / 2, 256), 256, 0, s>>>(x, y_soft, y_hw, n);
   return cudaGetLastError();
 }
 

@@ -8,11 +8,19 @@
 // tile stays resident in one CTA while the query tiles of every shard pass it in ring
 // order (shard i = (j + k) mod P at step k for KV shard j), so dK and dV accumulate in
 // TMEM and leave once.  dQ partials are added into an fp32 accumulator in global memory.
+// Query tiles pass row index by row index: for t from the last tile down, the shards
+// i = (j + k) mod P in ring order (from this KV tile's starting step, u mod P, around) that
+// have a visible key for this KV tile.  The CTAs of a cohort (consecutive KV tiles of one
+// shard, launched side by side) read row t of every shard within P tiles of each other, so
+// each query tile and its dQ rows are fetched from DRAM about once per cohort rather than
+// once per CTA (at a million tokens a head's Q, dO and dQ accumulator are several times
+// the L2), while the spread starting steps keep the cohort's dQ reductions on different
+// tiles.
 //
 // One CTA = 128 keys (tile u of shard j) of one (batch, key/value head hk); query tiles of
 // 128 rows.  With grouped-query attention the G query heads h = hk*G + g that read this
-// key/value head pass one after another (g outermost, then the ring), so dK and dV sum
-// over the group in TMEM as they do over the ring.
+// key/value head pass one after another (g outermost, then the tile rows and the ring),
+// so dK and dV sum over the group in TMEM as they do over the ring.
 // Roles (640 threads):
 //   warp 0      producer: K, V once (TMA); per query tile Q, dO (TMA) and its 128 lse
 //               (log2 domain) and D values (bulk copies from the shard-major arrays the
@@ -37,6 +45,7 @@
 // TMEM columns: S^T/P^T [0,128), dP^T/dQ^T [128,256), dV [256,384), dK [384,512).
 #include <cuda_bf16.h>
 
+#include "ra_check.cuh"
 #include "ra_internal.h"
 #include "ra_ptx.cuh"
 #include "ra_rows.cuh"
@@ -103,7 +112,31 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-template <int D_>
+// Walk the query tiles (i, t) that see this CTA's KV tile, in the order of the schedule:
+//   TO (tile-outer; striped layout only): t from the last tile down to the first visible
+//     one, and for each t the query shards in ring order from the KV tile's starting step
+//     (in the striped layout query tile t sees KV tile u of every shard iff t >= u);
+//   otherwise the ring steps outermost, shard i = (j + k) mod P, and its visible query
+//     tiles t_lo(i) .. T - 1 inside.
+// f(i, t) handles one item and returns false to stop (a wait gave up).
+template <bool TO, class F>
+__device__ __forceinline__ bool bwd_walk(const BwdSched& sc, F&& f) {
+  if (TO) {
+    const int tmin = sc.t_lo(sc.j);
+    for (int t = sc.T - 1; t >= tmin; --t)
+      for (int kk = 0; kk < sc.P; ++kk)
+        if (!f(sc.i_of(sc.k_at(kk)), t)) return false;
+  } else {
+    for (int k = 0; k < sc.P; ++k) {
+      const int i = sc.i_of(k);
+      for (int t = sc.t_lo(i); t < sc.T; ++t)
+        if (!f(i, t)) return false;
+    }
+  }
+  return true;
+}
+
+template <int D_, bool TO>
 __global__ void __launch_bounds__(640, 1)
     ra_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -148,7 +181,13 @@ __global__ void __launch_bounds__(640, 1)
   const int bh = blockIdx.x / per_bh;
   const int idx = blockIdx.x % per_bh;
   int j, u;
-  if (a.layout == RA_LAYOUT_STRIPED || !a.causal) {
+  if (TO) {
+    // cohorts of kCohort KV tiles of one shard, heaviest (smallest u) first: a cohort's CTAs
+    // run side by side and, with the tile-outer walk, read each query tile at about the
+    // same time (one L2 fill serves the cohort when a head's Q, dO and dQ exceed the L2)
+    cohort_decode(idx, a.T, a.P, &u, &j);
+  } else if (a.layout == RA_LAYOUT_STRIPED || !a.causal) {
+    // the CTAs resident at once spread over every shard, heaviest (smallest u) first
     u = idx / a.P;
     j = idx % a.P;
   } else if (a.layout == RA_LAYOUT_ZIGZAG) {
@@ -161,7 +200,9 @@ __global__ void __launch_bounds__(640, 1)
     u = idx % a.T;
   }
   const int b = bh / a.Hkv, hk = bh % a.Hkv;
-  const BwdSched sc{j, u, a.n, a.T, a.P, a.layout, a.causal};
+  // tile-outer CTAs start their ring walk at step u mod P, so that a cohort spreads over
+  // the shards of each tile row (and its dQ reductions over different tiles)
+  const BwdSched sc{j, u, a.n, a.T, a.P, a.layout, a.causal, TO ? u % a.P : 0};
 
   if (threadIdx.x == 0) {
     *abort_flag = (*(volatile unsigned int*)a.err != 0u) ? 1u : 0u;
@@ -206,6 +247,9 @@ __global__ void __launch_bounds__(640, 1)
       tma_prefetch_desc(&tmDO);
       mbar_expect_tx(kv_full, 2 * C::VB);
       for (int cb = 0; cb < D_ / 64; ++cb) {
+        if (!check(a.err, rows_box_ok(cb * 64, hk, j, u * kTile, b, a.n, a.P, a.Hkv, a.B, D_),
+                   kChkTma))
+          continue;
         load_rows(sK + cb * kTile * 128, &tmK, kv_full, a.layout, cb * 64, hk, j, u * kTile, b,
                   a.n, a.P);
         load_rows(sV + cb * kTile * 128, &tmV, kv_full, a.layout, cb * 64, hk, j, u * kTile, b,
@@ -215,27 +259,28 @@ __global__ void __launch_bounds__(640, 1)
       bool ok = true;
       for (int g = 0; g < a.G && ok; ++g) {
         const int h = hk * a.G + g;
-        for (int k = 0; k < a.P && ok; ++k) {
-          const int i = sc.i_of(k);
-          for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
+        ok = bwd_walk<TO>(sc, [&](int i, int t) -> bool {
             const int st = m % NSTQ;
-            if (m >= NSTQ && !mbar_wait(&q_empty[st], ((m / NSTQ) - 1) & 1, wc)) {
-              ok = false;
-              break;
-            }
+            if (m >= NSTQ && !mbar_wait(&q_empty[st], ((m / NSTQ) - 1) & 1, wc)) return false;
             mbar_expect_tx(&q_full[st], 2 * C::QB + C::LDB);
-            for (int cb = 0; cb < D_ / 64; ++cb) {
-              load_rows(sQ + st * C::QB + cb * BQ * 128, &tmQ, &q_full[st], a.layout, cb * 64, h, i,
-                        t * BQ, b, a.n, a.P);
-              load_rows(sDO + st * C::QB + cb * BQ * 128, &tmDO, &q_full[st], a.layout, cb * 64, h,
-                        i, t * BQ, b, a.n, a.P);
-            }
             const size_t off = ld_base + (size_t)h * a.L + (size_t)i * a.n + (size_t)t * BQ;
-            bulk_load(sLD + st * (2 * BQ), a.lse + off, BQ * 4, &q_full[st]);
-            bulk_load(sLD + st * (2 * BQ) + BQ, a.Dvec + off, BQ * 4, &q_full[st]);
-          }
-        }
+            if (check(a.err, rows_box_ok(0, h, i, t * BQ, b, a.n, a.P, a.H, a.B, D_) &&
+                                 off + BQ <= (size_t)a.B * a.H * a.L && st < NSTQ,
+                      kChkTma)) {
+              for (int cb = 0; cb < D_ / 64; ++cb) {
+                load_rows(sQ + st * C::QB + cb * BQ * 128, &tmQ, &q_full[st], a.layout, cb * 64,
+                          h, i, t * BQ, b, a.n, a.P);
+                load_rows(sDO + st * C::QB + cb * BQ * 128, &tmDO, &q_full[st], a.layout,
+                          cb * 64, h, i, t * BQ, b, a.n, a.P);
+              }
+              bulk_load(sLD + st * (2 * BQ), a.lse + off, BQ * 4, &q_full[st]);
+              bulk_load(sLD + st * (2 * BQ) + BQ, a.Dvec + off, BQ * 4, &q_full[st]);
+            }
+            ++m;
+            return true;
+        });
       }
+      if (kChecked) misc[2] = m;                 // items loaded, compared at the exit
       // let every copy this thread issued land before the CTA can exit
       mbar_wait_drain(kv_full, 0, a.wait_limit_ns);
       for (int r = (m > NSTQ ? m - NSTQ : 0); r < m; ++r)
@@ -259,6 +304,10 @@ __global__ void __launch_bounds__(640, 1)
       const uint64_t dsMN = sdesc_mnmajor(ds_addr, kTile * 128);   // dS^T: N = queries
       bool ok = mbar_wait(kv_full, 0, wc);
       tc_fence_after();
+      // S^T, dP^T, dV and dK inside the allocation and disjoint
+      if (!check(a.err, C::COL_S + 128 <= C::COL_DP && C::COL_DP + 128 <= C::COL_DV &&
+                            C::COL_DV + D_ <= C::COL_DK && C::COL_DK + D_ <= 512, kChkTmem))
+        ok = false;
       int total = 0;
       for (int k = 0; k < a.P; ++k) total += sc.T - sc.t_lo(sc.i_of(k));
       total *= a.G;
@@ -327,6 +376,7 @@ __global__ void __launch_bounds__(640, 1)
         umma_commit(&q_empty[st]);  // Q(m), dO(m) read for the last time
       }
 #undef RA_SCORES
+      if (kChecked) misc[3] = total;             // compared at the exit
       umma_commit(kv_final);
       umma_commit(drain);
       if (!ok) mbar_wait_drain(drain, 0, a.wait_limit_ns);
@@ -341,19 +391,18 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tDP = tbase + lane_off + C::COL_DP + 64 * half;
     const float sl2 = a.scale_log2;
     uint8_t* drow = sDS + half * (kTile * 128) + brow * 128;
-    bool ok = true;
+    // this thread's S^T, dP^T columns and its dS^T row: inside the allocation, the warp's
+    // lane quarter and the dS^T tile
+    bool ok = check(a.err, tmem_ok(tS, tbase, 64, warp) && tmem_ok(tDP, tbase, 64, warp) &&
+                               drow + 128 <= sDS + C::SB, kChkTmem | kChkSmem);
     int m = 0;
     for (int g = 0; g < a.G && ok; ++g) {
-      for (int k = 0; k < a.P && ok; ++k) {
-        const int i = sc.i_of(k);
-        for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
+      ok = bwd_walk<TO>(sc, [&](int i, int t) -> bool {
           const int st = m % NSTQ;
-          if (!mbar_wait(s_full, m & 1, wc) || !mbar_wait(&q_full[st], (m / NSTQ) & 1, wc)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(s_full, m & 1, wc) || !mbar_wait(&q_full[st], (m / NSTQ) & 1, wc))
+            return false;
           // dS^T(m) overwrites the shared tile once dQ^T(m-1) and dK(m-1) have read it
-          if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) { ok = false; break; }
+          if (m >= 1 && !mbar_wait(ds_free, (m - 1) & 1, wc)) return false;
           tc_fence_after();
           const float* lse2 = sLD + st * (2 * BQ) + 64 * half;   // -lse * log2(e)
           const float* dvec = lse2 + BQ;                          // -D
@@ -416,9 +465,11 @@ __global__ void __launch_bounds__(640, 1)
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(ds_ready);
-        }
-      }
+          ++m;
+          return true;
+      });
     }
+    if (kChecked && brow == 0) misc[4 + half] = m;   // compared at the exit
     // ---- dK, dV epilogue (thread = key row): warpgroup 0 writes dV, 1 writes dK ------
     if (ok && mbar_wait(kv_final, 0, wc)) {
       tc_fence_after();
@@ -429,8 +480,11 @@ __global__ void __launch_bounds__(640, 1)
       const uint32_t tcol = tbase + lane_off + (half ? C::COL_DK : C::COL_DV);
       const float mul = half ? a.scale : 1.f;
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(half ? a.dk : a.dv) + row * D_;
+      const bool in_range = check(a.err, tok >= 0 && tok < a.L && row < (size_t)a.B * a.L * a.Hkv &&
+                                             tmem_ok(tcol, tbase, D_, warp),
+                                  kChkGlobal);
 #pragma unroll
-      for (int c = 0; c < D_ / 32; ++c) {
+      for (int c = 0; c < (in_range ? D_ / 32 : 0); ++c) {
         uint32_t r[32];
         tmem_ld32(tcol + 32 * c, r);
         tmem_wait_ld();
@@ -454,15 +508,13 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tQ = tbase + (static_cast<uint32_t>(wq * 32) << 16) + C::COL_DP + 64 * half;
     const long long qstride = (a.layout == RA_LAYOUT_STRIPED) ? (long long)a.P * a.H * D_
                                                               : (long long)a.H * D_;
-    bool ok = true;
+    bool ok = check(a.err, tmem_ok(tQ, tbase, 64, warp), kChkTmem);
     int m = 0;
     for (int g = 0; g < a.G && ok; ++g) {
       float* dq_head =
           a.dq_acc + (size_t)b * a.L * a.H * D_ + (size_t)(hk * a.G + g) * D_ + drow;
-      for (int k = 0; k < a.P && ok; ++k) {
-        const int i = sc.i_of(k);
-        for (int t = sc.t_lo(i); t < sc.T; ++t, ++m) {
-          if (!mbar_wait(dq_full, m & 1, wc)) { ok = false; break; }
+      ok = bwd_walk<TO>(sc, [&](int i, int t) -> bool {
+          if (!mbar_wait(dq_full, m & 1, wc)) return false;
           tc_fence_after();
           uint32_t q0[32], q1[32];
           tmem_ld32(tQ, q0);
@@ -470,21 +522,35 @@ __global__ void __launch_bounds__(640, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(dq_empty);
-          if (drow >= D_) continue;   // a zero row of the padded K (D_ = 64)
+          ++m;
+          if (drow >= D_) return true;   // a zero row of the padded K (D_ = 64)
           // 64 consecutive local rows: consecutive tokens (stride qstride) in every layout
           const long long tok0 = token_of(a.layout, i, t * BQ + 64 * half, a.n, a.P);
           float* p0 = dq_head + tok0 * a.H * D_;
+          // the 64 rows' elements inside the accumulator (first and last token, the head)
+          if (!check(a.err, tok0 >= 0 && tok0 + 63 * (qstride / (a.H * D_)) < a.L &&
+                                hk * a.G + g < a.H &&
+                                token_of(a.layout, i, t * BQ + 64 * half + 63, a.n, a.P) ==
+                                    tok0 + 63 * (qstride / (a.H * D_)),
+                     kChkGlobal))
+            return true;
 #pragma unroll
           for (int c = 0; c < 32; ++c) red_add_f32(p0 + c * qstride, __uint_as_float(q0[c]));
 #pragma unroll
           for (int c = 0; c < 32; ++c) red_add_f32(p0 + (32 + c) * qstride, __uint_as_float(q1[c]));
-        }
-      }
+          return true;
+      });
     }
+    if (kChecked && drow == 0) misc[6 + half] = m;   // compared at the exit
   }
 
   tc_fence_before();
   __syncthreads();
+  if (kChecked && threadIdx.x == 0 && !*abort_flag)
+    // the producer, the MMA issuer, both key-row and both drain warpgroups walked the
+    // same number of query tiles
+    check(a.err, misc[2] == misc[3] && misc[4] == misc[3] && misc[5] == misc[3] &&
+                     misc[6] == misc[3] && misc[7] == misc[3], kChkSched);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
@@ -493,23 +559,29 @@ __global__ void __launch_bounds__(640, 1)
 
 }  // namespace
 
-template <int D_>
+template <int D_, bool TO>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(ra_bwd_kernel<D_>,
+  cudaError_t e = cudaFuncSetAttribute(ra_bwd_kernel<D_, TO>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BwdCfg<D_>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.B * a.Hkv * a.P * a.T;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ra_bwd_kernel<D_><<<(unsigned)grid, 640, BwdCfg<D_>::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  ra_bwd_kernel<D_, TO><<<(unsigned)grid, 640, BwdCfg<D_>::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
-  if (a.D == 128) return launch_bwd_d<128>(a, tq, tk, tv, tdo, s);
-  if (a.D == 64) return launch_bwd_d<64>(a, tq, tk, tv, tdo, s);
+  // tile-outer walk and cohort launch order for the striped layout once a head's Q, dO
+  // and fp32 dQ accumulator outgrow half the L2 (there the default order re-reads them)
+  const bool to = a.layout == RA_LAYOUT_STRIPED &&
+                  8.0 * (double)a.L * a.D >= (double)kTileOuterBytes;
+  if (a.D == 128) return to ? launch_bwd_d<128, true>(a, tq, tk, tv, tdo, s)
+                            : launch_bwd_d<128, false>(a, tq, tk, tv, tdo, s);
+  if (a.D == 64) return to ? launch_bwd_d<64, true>(a, tq, tk, tv, tdo, s)
+                           : launch_bwd_d<64, false>(a, tq, tk, tv, tdo, s);
   return cudaErrorNotSupported;
 }
 

@@ -6,7 +6,11 @@
 //     sum = sum * correction + rowsum(exp(s - new_max)), acc = acc * correction + P V;
 //     finally out = acc / sum;
 //   * ring order, section "リングトポロジーと KV の循環" (and the vanos001 ring diagram):
-//     the queries of shard i visit KV shards (i - k) mod P for k = 0..P-1;
+//     the queries of shard i visit KV shards (i - k) mod P for k = 0..P-1; here tile index
+//     by tile index: for u = 0, 1, ..., the ring's shards in that order, each KV tile u
+//     with a visible key (so that a cohort of CTAs of one shard, launched side by side,
+//     reads each K/V tile from DRAM once: at a million tokens a head's K and V are several
+//     times the L2);
 //   * causal skipping, section "Causal Masking の処理": KV tiles after the query tile
 //     are skipped, the diagonal tile is masked, earlier tiles are not.
 //
@@ -35,6 +39,8 @@
 // bf16 for the tensor core.
 #include <cuda_bf16.h>
 
+#include "ra_check.cuh"
+#include "ra_exp2.cuh"
 #include "ra_internal.h"
 #include "ra_ptx.cuh"
 #include "ra_rows.cuh"
@@ -44,6 +50,10 @@ namespace ra {
 namespace {
 
 constexpr float kTau = 8.0f;
+// One column pair in every kSoftExpEvery takes its exponentials in software on the FMA
+// pipe (ra_exp2.cuh) instead of the exponential unit, which the softmax keeps busy;
+// 0 = all on the exponential unit.
+constexpr int kSoftExpEvery = 0;
 constexpr float kNegInf = -__builtin_huge_valf();
 
 template <int D>
@@ -118,7 +128,10 @@ __device__ void count_work(const FwdArgs& a, const RingSched& sc, int g) {
   }
 }
 
-template <int D>
+// TO (tile-outer; striped layout only): every role walks KV tile index u outermost and
+// the ring steps inside, and the CTAs are launched in cohorts of one shard (see the decode
+// below).  Otherwise the ring steps are outermost and the KV tiles of a step inside.
+template <int D, bool TO>
 __global__ void __launch_bounds__(384, 1)
     ra_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -167,15 +180,32 @@ __global__ void __launch_bounds__(384, 1)
     const int ch = pos / hp;
     i = ch < a.P ? ch : 2 * a.P - 1 - ch;
     s = (ch < a.P ? 0 : hp) + pos % hp;
+  } else if (TO) {
+    // cohorts of kCohort tile pairs of one shard, heaviest first: a cohort's CTAs run
+    // side by side and, with the tile-outer walk, read every K/V tile at about the same
+    // time (one L2 fill serves the cohort when a head's K and V exceed the L2)
+    int rank;
+    cohort_decode(idx, a.npair, a.P, &rank, &i);
+    s = a.npair - 1 - rank;
   } else {
+    // the CTAs resident at once spread over every shard of the head
     s = a.npair - 1 - idx / a.P;
     i = idx % a.P;
   }
   const int b = bh / a.H, h = bh % a.H;
   const int hkv = h / a.G;        // key/value head of this query head
   const int steps = a.P / a.n_split;
-  RingSched sc{i, 2 * s, 2, a.T, a.P, a.layout, a.causal, g * steps, (g + 1) * steps};
+  // tile-outer CTAs start their ring walk at step s mod steps, so that a cohort spreads
+  // over the shards of each tile row
+  RingSched sc{i, 2 * s, 2, a.T, a.P, a.layout, a.causal, g * steps, (g + 1) * steps,
+               TO ? s % steps : 0};
   const int nvalid = (2 * s + 1 < a.T) ? 2 : 1;
+  // Every role walks the same items, (u, j) pairs with a visible key for either query tile:
+  //   ring steps outermost (KV shard j = (i - k) mod P), then u = 0 .. u_end(j) - 1; or
+  //   (TO, striped) u = 0 .. umax - 1 outermost, then the ring steps; in the striped layout
+  //   query tile t sees KV tiles u <= t of every shard (u == t masked), so every (u, j)
+  //   with u < umax is an item and each query tile's visible prefix is the same for all j.
+  const int umax = sc.u_max();
 
   if (threadIdx.x == 0) {
     *abort_flag = (*(volatile unsigned int*)a.err != 0u) ? 1u : 0u;
@@ -224,23 +254,36 @@ __global__ void __launch_bounds__(384, 1)
         mbar_expect_tx(q_full, nvalid * C::QB);
         for (int q = 0; q < nvalid; ++q)
           for (int cb = 0; cb < C::NCB; ++cb)
-            load_rows(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h, i,
-                      (2 * s + q) * kTile, b, a.n, a.P);
+            if (check(a.err, rows_box_ok(cb * 64, h, i, (2 * s + q) * kTile, b, a.n, a.P, a.H,
+                                         a.B, D), kChkTma))
+              load_rows(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h,
+                        i, (2 * s + q) * kTile, b, a.n, a.P);
       }
       int n = 0;
       bool ok = true;
-      for (int k = sc.k0; k < sc.k1 && ok; ++k) {
-        const int j = sc.j_of(k);
-        const int ue = sc.u_end(j);
-        for (int u = 0; u < ue; ++u, ++n) {
-          const int st = n % NS;
-          if (n >= NS && !mbar_wait(&empty[st], ((n / NS) - 1) & 1, wc)) { ok = false; break; }
-          mbar_expect_tx(&full[st], C::KVB);
-          for (int cb = 0; cb < C::NCB; ++cb)
+      auto item = [&](int u, int j) {
+        const int st = n % NS;
+        if (n >= NS && !mbar_wait(&empty[st], ((n / NS) - 1) & 1, wc)) return false;
+        mbar_expect_tx(&full[st], C::KVB);
+        for (int cb = 0; cb < C::NCB; ++cb)
+          if (check(a.err, rows_box_ok(cb * 64, hkv, j, u * kTile, b, a.n, a.P, a.H / a.G, a.B,
+                                       D) && st < NS, kChkTma))
             load_rows(ring + st * C::KVB + cb * kTile * 128, tm, &full[st], a.layout, cb * 64,
                       hkv, j, u * kTile, b, a.n, a.P);
+        ++n;
+        return true;
+      };
+      if (TO) {
+        for (int u = 0; u < umax && ok; ++u)
+          for (int kk = 0; kk < steps && ok; ++kk) ok = item(u, sc.j_of(sc.k_at(kk)));
+      } else {
+        for (int kk = 0; kk < steps && ok; ++kk) {
+          const int j = sc.j_of(sc.k_at(kk));
+          const int ue = sc.u_end(j);
+          for (int u = 0; u < ue && ok; ++u) ok = item(u, j);
         }
       }
+      if (kChecked) misc[is_k ? 2 : 3] = n;     // items loaded, compared at the exit
       // let every copy this thread issued land before the CTA can exit
       if (is_k) mbar_wait_drain(q_full, 0, a.wait_limit_ns);
       for (int m = (n > NS ? n - NS : 0); m < n; ++m)
@@ -262,6 +305,10 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t q0d = sdesc_kmajor(q_addr), q1d = sdesc_kmajor(q_addr + C::QB);
       const uint32_t dS0 = tbase + C::COL_S, dS1 = tbase + C::COL_S + 128;
       const uint32_t dO0 = tbase + C::COL_O, dO1 = tbase + C::COL_O + D;
+      // the four accumulators inside the allocation, S columns disjoint from O columns
+      if (!check(a.err, C::COL_S + 256 <= C::COL_O && C::COL_O + 2 * D <= 512, kChkTmem))
+        ok = false;
+      int n_s0 = 0, n_s1 = 0;
 
 #define RA_ISSUE_PV(PEND, PPAR, PV, PFULL, DO_, AP_)                                          \
   do {                                                                                        \
@@ -287,35 +334,50 @@ __global__ void __launch_bounds__(384, 1)
   } while (0)
 
       int n = 0;
-      for (int k = sc.k0; k < sc.k1 && ok; ++k) {
-        const int j = sc.j_of(k);
-        const int ue0 = sc.q_end(0, j), ue1 = sc.q_end(1, j);
-        const int ue = ue0 > ue1 ? ue0 : ue1;
-        for (int u = 0; u < ue; ++u, ++n) {
+      // one item: the S MMA of each query tile that sees KV tile u (u < ue_q), each after
+      // the PV of that tile's previous item
+      auto item = [&](int u, int ue0, int ue1) -> bool {
           const int kst = n % NK, vst = n % NV;
-          if (!mbar_wait(&k_full[kst], (n / NK) & 1, wc)) { ok = false; break; }
+          if (!mbar_wait(&k_full[kst], (n / NK) & 1, wc)) return false;
           tc_fence_after();
           const uint64_t kd = sdesc_kmajor(k_addr + kst * C::KVB);
           // query tile 0
           if (pend0 >= 0) RA_ISSUE_PV(pend0, ppar0, pv0, &p_full[0], dO0, dS0);
-          if (!ok) break;
+          if (!ok) return false;
+          if (!check(a.err, kst < NK && vst < NV, kChkSmem)) return false;
           if (u < ue0) {
             RA_ISSUE_S(q0d, dS0);
+            ++n_s0;
             umma_commit(&s_full[0]);
             pend0 = vst;
             ppar0 = (n / NV) & 1;
           }
           // query tile 1
           if (pend1 >= 0) RA_ISSUE_PV(pend1, ppar1, pv1, &p_full[1], dO1, dS1);
-          if (!ok) break;
+          if (!ok) return false;
           if (u < ue1) {
             RA_ISSUE_S(q1d, dS1);
+            ++n_s1;
             umma_commit(&s_full[1]);
             pend1 = vst;
             ppar1 = (n / NV) & 1;
           }
           umma_commit(&k_empty[kst]);                       // both S MMAs of item n issued
           if (n > 0) umma_commit(&v_empty[(n - 1) % NV]);    // every PV of item n-1 issued
+          ++n;
+          return true;
+      };
+      if (TO) {
+        // striped: each query tile sees the same prefix of every shard
+        const int ue0 = sc.q_end(0, i), ue1 = sc.q_end(1, i);
+        for (int u = 0; u < umax && ok; ++u)
+          for (int kk = 0; kk < steps && ok; ++kk) ok = item(u, ue0, ue1);
+      } else {
+        for (int kk = 0; kk < steps && ok; ++kk) {
+          const int j = sc.j_of(sc.k_at(kk));
+          const int ue0 = sc.q_end(0, j), ue1 = sc.q_end(1, j);
+          const int ue = ue0 > ue1 ? ue0 : ue1;
+          for (int u = 0; u < ue && ok; ++u) ok = item(u, ue0, ue1);
         }
       }
       if (ok && pend0 >= 0) RA_ISSUE_PV(pend0, ppar0, pv0, &p_full[0], dO0, dS0);
@@ -323,6 +385,11 @@ __global__ void __launch_bounds__(384, 1)
       if (ok && n > 0) umma_commit(&v_empty[(n - 1) % NV]);
 #undef RA_ISSUE_PV
 #undef RA_ISSUE_S
+      if (kChecked) {                           // compared at the exit
+        misc[4] = n;
+        misc[5] = n_s0;
+        misc[6] = n_s1;
+      }
       umma_commit(&o_final[0]);
       umma_commit(&o_final[1]);
       umma_commit(drain);
@@ -344,13 +411,12 @@ __global__ void __launch_bounds__(384, 1)
     const float tau_raw = kTau / sl2;           // rescale threshold in raw score units
     float m_run = kNegInf, l_run = 0.f;         // running max (raw units) and row sum
     int cnt = 0;
-    bool ok = true;
-    if (valid) {
-      for (int k = sc.k0; k < sc.k1 && ok; ++k) {
-        const int j = sc.j_of(k);
-        const int ueq = sc.q_end(q, j), udiag = sc.q_diag(q, j);
-        for (int u = 0; u < ueq; ++u) {
-          if (!mbar_wait(&s_full[q], cnt & 1, wc)) { ok = false; break; }
+    // this thread's S/P and O columns: inside the allocation and the warp's lane quarter
+    bool ok = check(a.err, tmem_ok(tS, tbase, 128, warp) && tmem_ok(tO, tbase, D, warp),
+                    kChkTmem);
+    // one item: the scores of KV tile u of shard j (masked when on_diag)
+    auto item = [&](bool on_diag, int j) -> bool {
+          if (!mbar_wait(&s_full[q], cnt & 1, wc)) return false;
           tc_fence_after();
           // all four 32-column loads in flight before the one wait
           float sv[128];
@@ -369,7 +435,7 @@ __global__ void __launch_bounds__(384, 1)
               sv[96 + e] = __uint_as_float(r3[e]);
             }
           }
-          if (u == udiag) {
+          if (on_diag) {
             const int lim = arow - ((a.layout == RA_LAYOUT_STRIPED && j > i) ? 1 : 0);
 #pragma unroll
             for (int e = 0; e < 128; ++e)
@@ -408,7 +474,13 @@ __global__ void __launch_bounds__(384, 1)
               float x0, x1;
               f2_unpack(f2_mul(f2_add(f2_pack(sv[32 * c + 2 * e], sv[32 * c + 2 * e + 1]), nm2), c2),
                         x0, x1);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              float p0, p1;
+              if (kSoftExpEvery > 0 && e % kSoftExpEvery == kSoftExpEvery - 1) {
+                f2_unpack(exp2_soft_x2(x0, x1), p0, p1);     // on the FMA pipe
+              } else {
+                p0 = ex2_approx(x0);
+                p1 = ex2_approx(x1);
+              }
               acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(p0, p1));
               pk[e] = pack_bf16x2(p0, p1);
             }
@@ -437,9 +509,24 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_before();
           mbar_arrive(&p_full[q]);
           ++cnt;
+          return true;
+    };
+    if (valid) {
+      if (TO) {
+        // striped: the same visible prefix and diagonal tile in every shard
+        const int ueq = sc.q_end(q, i), udiag = sc.q_diag(q, i);
+        for (int u = 0; u < ueq && ok; ++u)
+          for (int kk = 0; kk < steps; ++kk)
+            if (!item(u == udiag, sc.j_of(sc.k_at(kk)))) { ok = false; break; }
+      } else {
+        for (int kk = 0; kk < steps && ok; ++kk) {
+          const int j = sc.j_of(sc.k_at(kk));
+          const int ueq = sc.q_end(q, j), udiag = sc.q_diag(q, j);
+          for (int u = 0; u < ueq; ++u) if (!item(u == udiag, j)) { ok = false; break; }
         }
       }
     }
+    if (kChecked && arow == 0) misc[7 + q] = cnt;   // compared at the exit
     if (ok && mbar_wait(&o_final[q], 0, wc) && valid) {
       tc_fence_after();
       const int loc = t * kTile + arow;
@@ -450,18 +537,22 @@ __global__ void __launch_bounds__(384, 1)
           l_run == 0.f ? kNegInf : (m_run * sl2 + __log2f(l_run)) * 0.69314718055994531f;
       const size_t row = ((size_t)b * a.L + tok) * a.H + h;
       const size_t lidx = ((size_t)b * a.H + h) * a.L + tok;
+      const bool in_range = check(
+          a.err, tok >= 0 && tok < a.L && (row + 1) * D <= (size_t)a.B * a.L * a.H * D &&
+                     lidx < (size_t)a.B * a.H * a.L && g < a.n_split,
+          kChkGlobal);
       float* of32 = nullptr;
       __nv_bfloat16* obf = nullptr;
-      if (a.n_split > 1) {
+      if (in_range && a.n_split > 1) {
         of32 = a.o_part + (size_t)g * a.B * a.L * a.H * D + row * D;
         a.lse_part[(size_t)g * a.B * a.H * a.L + lidx] = lse_v;
-      } else {
+      } else if (in_range) {
         if (a.out_fp32) of32 = reinterpret_cast<float*>(a.out) + row * D;
         else obf = reinterpret_cast<__nv_bfloat16*>(a.out) + row * D;
         a.lse[lidx] = lse_v;
       }
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < (in_range ? D / 32 : 0); ++c) {
         uint32_t r[32];
         tmem_ld32(tO + 32 * c, r);
         tmem_wait_ld();
@@ -490,22 +581,27 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kChecked && threadIdx.x == 0 && !*abort_flag)
+    // both producers and the MMA issuer walked the same items; each softmax warpgroup saw
+    // as many score tiles as the MMA issuer computed for its query tile
+    check(a.err, misc[2] == misc[3] && misc[3] == misc[4] && misc[5] == misc[7] &&
+                     misc[6] == misc[8], kChkSched);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
 }
 
-template <int D>
+template <int D, bool TO>
 cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t st) {
   using C = FwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(ra_fwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(ra_fwd_kernel<D, TO>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.B * a.H * a.P * a.npair * a.n_split;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ra_fwd_kernel<D><<<(unsigned)grid, 384, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
+  ra_fwd_kernel<D, TO><<<(unsigned)grid, 384, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -513,8 +609,13 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensor
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
-  if (a.D == 64) return launch_fwd_d<64>(a, tq, tk, tv, s);
-  return launch_fwd_d<128>(a, tq, tk, tv, s);
+  // tile-outer walk and cohort launch order for the striped layout once a key/value
+  // head's K and V outgrow half the L2 (there the default order re-reads them from DRAM)
+  const bool to = a.layout == RA_LAYOUT_STRIPED &&
+                  4.0 * (double)a.L * a.D >= (double)kTileOuterBytes;
+  if (a.D == 64) return to ? launch_fwd_d<64, true>(a, tq, tk, tv, s)
+                           : launch_fwd_d<64, false>(a, tq, tk, tv, s);
+  return to ? launch_fwd_d<128, true>(a, tq, tk, tv, s) : launch_fwd_d<128, false>(a, tq, tk, tv, s);
 }
 
 }  // namespace ra

@@ -25,6 +25,7 @@
 // variance, two passes over the row held in registers; 128 threads per row.
 #include <cuda_bf16.h>
 
+#include "ra_check.cuh"
 #include "ra_internal.h"
 #include "ra_layer.h"
 #include "ra_ptx.cuh"
@@ -161,6 +162,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           mbar_expect_tx(&full[s], kAB + kBB);
+          // the tile's boxes inside A [M, K] and B [N, K]
+          if (!check(g.err, tm >= 0 && (tm + 1) * GM <= g.M && tn >= 0 && (tn + 1) * GN <= g.N &&
+                                (kb + 1) * GK <= g.K && s < kStages, kChkTma))
+            continue;
           // K-major: one box of rows x 64 K; MN-major: boxes of 64 K rows x 64 M (or N)
           if (A_MN) {
 #pragma unroll
@@ -178,6 +183,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
+      if (kChecked) misc[2] = it;                // K steps loaded, compared at the exit
       // let every copy this thread issued land before the CTA can exit
       for (int r = (it > kStages ? it - kStages : 0); r < it; ++r)
         wait_drain(&full[r % kStages], (r / kStages) & 1, g.wait_limit_ns);
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int pid = blockIdx.x; pid < ntiles && ok; pid += gridDim.x, ++lt) {
         const int buf = lt & 1;
         const uint32_t tacc = tbase + buf * GN;
+        if (!check(g.err, buf * GN + GN <= 512, kChkTmem)) { ok = false; break; }
         // the epilogue has read this accumulator's previous tile out of TMEM
         if (lt >= 2 && !mbar_wait(&acc_empty[buf], ((lt >> 1) - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
@@ -211,6 +218,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (ok) umma_commit(&acc_full[buf]);
       }
+      if (kChecked) misc[3] = it;                // compared at the exit
       umma_commit(drain);
       wait_drain(drain, 0, g.wait_limit_ns);     // every MMA done before TMEM is released
     }
@@ -226,6 +234,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t trow = tbase + buf * GN + (static_cast<uint32_t>(q * 32) << 16);
       const size_t row = (size_t)tm * GM + r;
       if (!mbar_wait(&acc_full[buf], (lt >> 1) & 1, wc)) break;
+      // the output rows and columns of this tile, and its TMEM accumulator
+      const bool in_range = check(g.err, row < (size_t)g.M && (size_t)(tn + 1) * GN <= (size_t)g.N &&
+                                             tmem_ok(trow, tbase, GN, warp),
+                                  kChkGlobal);
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < GN / 32; ++c) {
@@ -236,6 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_before();
           mbar_arrive(&acc_empty[buf]);
         }
+        if (!in_range) continue;
         const int col = tn * GN + 32 * c;
         const size_t e0 = row * g.N + col;
         float f[32];
@@ -308,6 +321,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kChecked && threadIdx.x == 0 && !*abort_flag)
+    check(g.err, misc[2] == misc[3], kChkSched);   // producer and MMA issuer agree
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);

@@ -27,4 +27,12 @@ __device__ __forceinline__ void load_rows(void* dst, const CUtensorMap* m, uint6
   }
 }
 
+// The box load_rows reads (64 features from d0, 128 local rows from local0, one head,
+// shard and batch) lies inside a [B, P * n, heads, D] tensor's shard view.
+__host__ __device__ inline bool rows_box_ok(int d0, int h, int shard, int local0, int b, int n,
+                                            int P, int heads, int B, int D) {
+  return d0 >= 0 && d0 + 64 <= D && h >= 0 && h < heads && shard >= 0 && shard < P &&
+         local0 >= 0 && local0 + 128 <= n && b >= 0 && b < B;
+}
+
 }  // namespace ra

@@ -51,7 +51,8 @@ typedef enum {
   RA_ERR_UNSUPPORTED = 2,     /* valid request this build has no kernel for       */
   RA_ERR_WORKSPACE = 3,       /* workspace null or smaller than *_workspace_bytes */
   RA_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed                */
-  RA_ERR_DEVICE_TIMEOUT = 5   /* a bounded wait inside a kernel ran out           */
+  RA_ERR_DEVICE_TIMEOUT = 5,  /* a bounded wait inside a kernel ran out           */
+  RA_ERR_CHECK = 6            /* checked build: a kernel found an index out of range */
 } ra_status_t;
 
 typedef enum {
@@ -219,7 +220,8 @@ ra_status_t ra_bwd_noalloc(const ra_params_t* p, const void* q, const void* k, c
                            void* dq, void* dk, void* dv, void* stream);
 
 /* Synchronises `stream`, reads the workspace's device error word, re-zeroes it, and
- * returns RA_ERR_DEVICE_TIMEOUT if a kernel gave up a wait since the last check. */
+ * returns RA_ERR_DEVICE_TIMEOUT if a kernel gave up a wait since the last check, and
+ * RA_ERR_CHECK if (checked build only) a kernel found an index out of range. */
 ra_status_t ra_check_error(void* workspace, void* stream);
 
 /* Diagnostic for the bounded-wait machinery: launches one CTA that waits on a
@@ -228,6 +230,24 @@ ra_status_t ra_check_error(void* workspace, void* stream);
  * stays usable).  ra_check_error() then returns RA_ERR_DEVICE_TIMEOUT. */
 ra_status_t ra_selftest_timeout(void* workspace, size_t workspace_bytes,
                                 unsigned int timeout_us, void* stream);
+
+/* Self-test of the two 2^x forms the softmax kernels mix (no counterpart on the pages,
+ * which take exp as given): for each of n fp32 inputs x[i] (device memory),
+ * y_soft[i] = the software form (range reduction and a polynomial on the FMA pipe,
+ * relative error below 4e-6; x <= -127 gives +0, NaN gives NaN) and y_hw[i] = the
+ * hardware unit's ex2.approx.ftz.  x, y_soft, y_hw: device fp32 arrays of n elements,
+ * caller-owned, 4-byte aligned; n in [1, 2^31).  Asynchronous on `stream`.  Returns
+ * RA_ERR_INVALID_ARG for null pointers or n out of range, RA_ERR_CUDA if the launch fails. */
+ra_status_t ra_selftest_exp2(const float* x, float* y_soft, float* y_hw, long long n,
+                             void* stream);
+
+/* 1 if this library is the checked build (compiled with RA_CHECKS, e.g. libra_checked.so),
+ * 0 otherwise.  In the checked build every kernel tests its tile and TMA box coordinates,
+ * TMEM columns and lane quarters, shared-memory operand offsets, global element indices
+ * and the per-role item counts before use; a violation skips the access, sets a bit of the
+ * workspace error word and ra_check_error() returns RA_ERR_CHECK.  It stands in for a
+ * memory checker; the pages have no counterpart. */
+int ra_checks_enabled(void);
 
 const char* ra_status_string(ra_status_t s);
 const char* ra_last_error_message(void);

@@ -338,3 +338,21 @@ def test_layer_parameter_rules_match_the_header(L):
         assert (api.lib().ra_bpt_train_workspace_bytes(ctypes.byref(prm)) > 0) == want_train
         seen[want] += 1
     assert seen[True] > 50 and seen[False] > 50
+
+
+def test_checked_build_links_and_exports_the_same_symbols(tmp_path):
+    """The checked build (compiled with RA_CHECKS) links, reports itself as checked and
+    exports every symbol the header declares; the normal build reports no checks."""
+    import ctypes
+    import shutil
+    from exact_blockwise_ring_gb300 import build
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("needs nvcc")
+    path = build.build(checked=True)
+    h = ctypes.CDLL(path)
+    h.ra_checks_enabled.restype = ctypes.c_int
+    assert h.ra_checks_enabled() == 1
+    for name in api.header_symbols():
+        assert hasattr(h, name), name
+    if not os.environ.get("RA_LIBRARY"):
+        assert api.lib().ra_checks_enabled() == 0

@@ -21,7 +21,7 @@ STRUCTS = {"ra_params_t": api.Params, "ra_bpt_params_t": api.BptParams,
            "ra_bpt_weights_t": api.BptWeights, "ra_bpt_grads_t": api.BptGrads}
 
 ENUMS = {"RA_OK": 0, "RA_ERR_INVALID_ARG": 1, "RA_ERR_UNSUPPORTED": 2, "RA_ERR_WORKSPACE": 3,
-         "RA_ERR_CUDA": 4, "RA_ERR_DEVICE_TIMEOUT": 5, "RA_LAYOUT_CONTIGUOUS": 0,
+         "RA_ERR_CUDA": 4, "RA_ERR_DEVICE_TIMEOUT": 5, "RA_ERR_CHECK": 6, "RA_LAYOUT_CONTIGUOUS": 0,
          "RA_LAYOUT_STRIPED": 1, "RA_LAYOUT_ZIGZAG": 2, "RA_BF16": api.RA_BF16,
          "RA_FP32": api.RA_FP32, "RA_EPI_BIAS": api.EPILOGUES["bias"],
          "RA_EPI_BIAS_GELU": api.EPILOGUES["bias_gelu"],

@@ -1,9 +1,10 @@
 """NaN and Inf inputs on the GPU: they propagate where the fp64 oracle puts them, every
 other output is unchanged, and no kernel waits in vain.
 
-labhub "Ring Attention 論文分析", section "限界と課題", names NaN/Inf from the online
-softmax as a hazard of the method.  A NaN in one element of q (row r) and, separately, +inf
-in one element of v (key c) are planted on the host; ra_fwd and ra_bwd then run on the
+labhub "Ring Attention 論文分析", section "限界、失敗事例、そして未解決の問題" (the failure
+case "NaN/Inf の発散"), names NaN/Inf from the online softmax as a hazard of the method.
+A NaN in one element of q (row r) and, separately, +inf in one element of v (key c) are
+planted on the host; ra_fwd and ra_bwd then run on the
 poisoned inputs in every layout, with the ring steps fused (one online state) and split
 (partials merged), and
 

@@ -1,8 +1,9 @@
 """Pins for the oracle on non-finite inputs (CPU only).
 
-labhub "Ring Attention 論文分析", section "限界と課題", names NaN/Inf arising in the
-online softmax as a hazard of the method.  A NaN or an infinity in an input must reach
-exactly the outputs that the definition makes depend on it, and no others:
+labhub "Ring Attention 論文分析", section "限界、失敗事例、そして未解決の問題" (the failure
+case "NaN/Inf の発散"), names NaN/Inf arising in the online softmax as a hazard of the
+method.  A NaN or an infinity in an input must reach exactly the outputs that the
+definition makes depend on it, and no others:
 
 * NaN in one element of q_r: every score of row r is NaN, so out_r, lse_r and dQ_r are NaN;
   row r's terms reach dK_c and dV_c of every key c <= r (causal), so those rows are NaN;
