@@ -8,14 +8,13 @@
 // tile stays resident in one CTA while the query tiles of every shard pass it in ring
 // order (shard i = (j + k) mod P at step k for KV shard j), so dK and dV accumulate in
 // TMEM and leave once.  dQ partials are added into an fp32 accumulator in global memory.
-// Query tiles pass row index by row index: for t from the last tile down, the shards
-// i = (j + k) mod P in ring order (from this KV tile's starting step, u mod P, around) that
-// have a visible key for this KV tile.  The CTAs of a cohort (consecutive KV tiles of one
-// shard, launched side by side) read row t of every shard within P tiles of each other, so
-// each query tile and its dQ rows are fetched from DRAM about once per cohort rather than
-// once per CTA (at a million tokens a head's Q, dO and dQ accumulator are several times
-// the L2), while the spread starting steps keep the cohort's dQ reductions on different
-// tiles.
+// For the striped layout at sizes where a head's Q, dO and dQ accumulator exceed half the
+// L2, query tiles pass row index by row index instead: for t from the last tile down, the
+// shards i = (j + k) mod P in ring order.  The CTAs launched side by side (the same KV tile
+// index u of every shard: the same work) then read row t of every shard within P tiles of
+// each other, so each query tile and its dQ rows are fetched from DRAM about once per
+// group rather than once per CTA (at a million tokens they are several times the L2),
+// while at each moment the group's dQ reductions land on different tiles.
 //
 // One CTA = 128 keys (tile u of shard j) of one (batch, key/value head hk); query tiles of
 // 128 rows.  With grouped-query attention the G query heads h = hk*G + g that read this
@@ -114,8 +113,8 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
 
 // Walk the query tiles (i, t) that see this CTA's KV tile, in the order of the schedule:
 //   TO (tile-outer; striped layout only): t from the last tile down to the first visible
-//     one, and for each t the query shards in ring order from the KV tile's starting step
-//     (in the striped layout query tile t sees KV tile u of every shard iff t >= u);
+//     one, and for each t the query shards in ring order (in the striped layout query tile
+//     t sees KV tile u of every shard iff t >= u);
 //   otherwise the ring steps outermost, shard i = (j + k) mod P, and its visible query
 //     tiles t_lo(i) .. T - 1 inside.
 // f(i, t) handles one item and returns false to stop (a wait gave up).
@@ -124,8 +123,8 @@ __device__ __forceinline__ bool bwd_walk(const BwdSched& sc, F&& f) {
   if (TO) {
     const int tmin = sc.t_lo(sc.j);
     for (int t = sc.T - 1; t >= tmin; --t)
-      for (int kk = 0; kk < sc.P; ++kk)
-        if (!f(sc.i_of(sc.k_at(kk)), t)) return false;
+      for (int k = 0; k < sc.P; ++k)
+        if (!f(sc.i_of(k), t)) return false;
   } else {
     for (int k = 0; k < sc.P; ++k) {
       const int i = sc.i_of(k);
@@ -181,13 +180,11 @@ __global__ void __launch_bounds__(640, 1)
   const int bh = blockIdx.x / per_bh;
   const int idx = blockIdx.x % per_bh;
   int j, u;
-  if (TO) {
-    // cohorts of kCohort KV tiles of one shard, heaviest (smallest u) first: a cohort's CTAs
-    // run side by side and, with the tile-outer walk, read each query tile at about the
-    // same time (one L2 fill serves the cohort when a head's Q, dO and dQ exceed the L2)
-    cohort_decode(idx, a.T, a.P, &u, &j);
-  } else if (a.layout == RA_LAYOUT_STRIPED || !a.causal) {
-    // the CTAs resident at once spread over every shard, heaviest (smallest u) first
+  if (a.layout == RA_LAYOUT_STRIPED || !a.causal) {
+    // consecutive CTAs: the same KV tile u (the same work) of every shard j, heaviest
+    // (smallest u) first.  With the tile-outer walk such a group runs in step and reads the
+    // same query tile row of every shard within P items of each other, so one L2 fill of
+    // Q, dO and the dQ rows serves the group.
     u = idx / a.P;
     j = idx % a.P;
   } else if (a.layout == RA_LAYOUT_ZIGZAG) {
@@ -200,9 +197,7 @@ __global__ void __launch_bounds__(640, 1)
     u = idx % a.T;
   }
   const int b = bh / a.Hkv, hk = bh % a.Hkv;
-  // tile-outer CTAs start their ring walk at step u mod P, so that a cohort spreads over
-  // the shards of each tile row (and its dQ reductions over different tiles)
-  const BwdSched sc{j, u, a.n, a.T, a.P, a.layout, a.causal, TO ? u % a.P : 0};
+  const BwdSched sc{j, u, a.n, a.T, a.P, a.layout, a.causal};
 
   if (threadIdx.x == 0) {
     *abort_flag = (*(volatile unsigned int*)a.err != 0u) ? 1u : 0u;
@@ -574,8 +569,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
-  // tile-outer walk and cohort launch order for the striped layout once a head's Q, dO
-  // and fp32 dQ accumulator outgrow half the L2 (there the default order re-reads them)
+  // tile-outer walk for the striped layout once a head's Q, dO and fp32 dQ accumulator
+  // outgrow half the L2 (there the default order re-reads them from DRAM)
   const bool to = a.layout == RA_LAYOUT_STRIPED &&
                   8.0 * (double)a.L * a.D >= (double)kTileOuterBytes;
   if (a.D == 128) return to ? launch_bwd_d<128, true>(a, tq, tk, tv, tdo, s)

@@ -6,11 +6,11 @@
 //     sum = sum * correction + rowsum(exp(s - new_max)), acc = acc * correction + P V;
 //     finally out = acc / sum;
 //   * ring order, section "リングトポロジーと KV の循環" (and the vanos001 ring diagram):
-//     the queries of shard i visit KV shards (i - k) mod P for k = 0..P-1; here tile index
-//     by tile index: for u = 0, 1, ..., the ring's shards in that order, each KV tile u
-//     with a visible key (so that a cohort of CTAs of one shard, launched side by side,
-//     reads each K/V tile from DRAM once: at a million tokens a head's K and V are several
-//     times the L2);
+//     the queries of shard i visit KV shards (i - k) mod P for k = 0..P-1 (for the
+//     striped layout at sizes where a head's K and V exceed half the L2, tile index by
+//     tile index: for u = 0, 1, ..., the ring's shards in that order; CTAs launched side
+//     by side then read each K/V tile row within a few items of each other, so one DRAM
+//     fill serves them: at a million tokens a head's K and V are several times the L2);
 //   * causal skipping, section "Causal Masking の処理": KV tiles after the query tile
 //     are skipped, the diagonal tile is masked, earlier tiles are not.
 //
@@ -129,8 +129,8 @@ __device__ void count_work(const FwdArgs& a, const RingSched& sc, int g) {
 }
 
 // TO (tile-outer; striped layout only): every role walks KV tile index u outermost and
-// the ring steps inside, and the CTAs are launched in cohorts of one shard (see the decode
-// below).  Otherwise the ring steps are outermost and the KV tiles of a step inside.
+// the ring steps inside.  Otherwise the ring steps are outermost and the KV tiles of a
+// step inside.
 template <int D, bool TO>
 __global__ void __launch_bounds__(384, 1)
     ra_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -180,31 +180,24 @@ __global__ void __launch_bounds__(384, 1)
     const int ch = pos / hp;
     i = ch < a.P ? ch : 2 * a.P - 1 - ch;
     s = (ch < a.P ? 0 : hp) + pos % hp;
-  } else if (TO) {
-    // cohorts of kCohort tile pairs of one shard, heaviest first: a cohort's CTAs run
-    // side by side and, with the tile-outer walk, read every K/V tile at about the same
-    // time (one L2 fill serves the cohort when a head's K and V exceed the L2)
-    int rank;
-    cohort_decode(idx, a.npair, a.P, &rank, &i);
-    s = a.npair - 1 - rank;
   } else {
-    // the CTAs resident at once spread over every shard of the head
+    // consecutive CTAs: the same tile pair s (the same work) of every shard i, heaviest
+    // first.  With the tile-outer walk such a group runs in step and reads the same KV tile
+    // row of every shard within P items of each other, so one L2 fill serves the group.
     s = a.npair - 1 - idx / a.P;
     i = idx % a.P;
   }
   const int b = bh / a.H, h = bh % a.H;
   const int hkv = h / a.G;        // key/value head of this query head
   const int steps = a.P / a.n_split;
-  // tile-outer CTAs start their ring walk at step s mod steps, so that a cohort spreads
-  // over the shards of each tile row
-  RingSched sc{i, 2 * s, 2, a.T, a.P, a.layout, a.causal, g * steps, (g + 1) * steps,
-               TO ? s % steps : 0};
+  RingSched sc{i, 2 * s, 2, a.T, a.P, a.layout, a.causal, g * steps, (g + 1) * steps};
   const int nvalid = (2 * s + 1 < a.T) ? 2 : 1;
   // Every role walks the same items, (u, j) pairs with a visible key for either query tile:
   //   ring steps outermost (KV shard j = (i - k) mod P), then u = 0 .. u_end(j) - 1; or
-  //   (TO, striped) u = 0 .. umax - 1 outermost, then the ring steps; in the striped layout
-  //   query tile t sees KV tiles u <= t of every shard (u == t masked), so every (u, j)
-  //   with u < umax is an item and each query tile's visible prefix is the same for all j.
+  //   (TO, striped) u = 0 .. umax - 1 outermost, then the ring steps in ring order; in the
+  //   striped layout query tile t sees KV tiles u <= t of every shard (u == t masked), so
+  //   every (u, j) with u < umax is an item and each query tile's visible prefix is the
+  //   same for all j.
   const int umax = sc.u_max();
 
   if (threadIdx.x == 0) {
@@ -275,10 +268,10 @@ __global__ void __launch_bounds__(384, 1)
       };
       if (TO) {
         for (int u = 0; u < umax && ok; ++u)
-          for (int kk = 0; kk < steps && ok; ++kk) ok = item(u, sc.j_of(sc.k_at(kk)));
+          for (int kk = 0; kk < steps && ok; ++kk) ok = item(u, sc.j_of(sc.k0 + kk));
       } else {
         for (int kk = 0; kk < steps && ok; ++kk) {
-          const int j = sc.j_of(sc.k_at(kk));
+          const int j = sc.j_of(sc.k0 + kk);
           const int ue = sc.u_end(j);
           for (int u = 0; u < ue && ok; ++u) ok = item(u, j);
         }
@@ -374,7 +367,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int kk = 0; kk < steps && ok; ++kk) ok = item(u, ue0, ue1);
       } else {
         for (int kk = 0; kk < steps && ok; ++kk) {
-          const int j = sc.j_of(sc.k_at(kk));
+          const int j = sc.j_of(sc.k0 + kk);
           const int ue0 = sc.q_end(0, j), ue1 = sc.q_end(1, j);
           const int ue = ue0 > ue1 ? ue0 : ue1;
           for (int u = 0; u < ue && ok; ++u) ok = item(u, ue0, ue1);
@@ -517,10 +510,10 @@ __global__ void __launch_bounds__(384, 1)
         const int ueq = sc.q_end(q, i), udiag = sc.q_diag(q, i);
         for (int u = 0; u < ueq && ok; ++u)
           for (int kk = 0; kk < steps; ++kk)
-            if (!item(u == udiag, sc.j_of(sc.k_at(kk)))) { ok = false; break; }
+            if (!item(u == udiag, sc.j_of(sc.k0 + kk))) { ok = false; break; }
       } else {
         for (int kk = 0; kk < steps && ok; ++kk) {
-          const int j = sc.j_of(sc.k_at(kk));
+          const int j = sc.j_of(sc.k0 + kk);
           const int ueq = sc.q_end(q, j), udiag = sc.q_diag(q, j);
           for (int u = 0; u < ueq; ++u) if (!item(u == udiag, j)) { ok = false; break; }
         }
@@ -609,8 +602,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensor
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
-  // tile-outer walk and cohort launch order for the striped layout once a key/value
-  // head's K and V outgrow half the L2 (there the default order re-reads them from DRAM)
+  // tile-outer walk for the striped layout once a key/value head's K and V outgrow half
+  // the L2 (there the default order re-reads them from DRAM)
   const bool to = a.layout == RA_LAYOUT_STRIPED &&
                   4.0 * (double)a.L * a.D >= (double)kTileOuterBytes;
   if (a.D == 64) return to ? launch_fwd_d<64, true>(a, tq, tk, tv, s)

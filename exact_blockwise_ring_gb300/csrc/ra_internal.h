@@ -85,35 +85,10 @@ __host__ __device__ inline long long tokens_upto(int layout, int j, long long to
   return blocks_upto(layout, j, tok, n, P);   // blocks of one token
 }
 
-// CTAs that run side by side read the same tiles at the same time only if they belong to
-// one shard and walk their tiles in one order; kCohort consecutive units of a shard form
-// such a cohort.
-constexpr int kCohort = 16;
 // A head's streamed operands at or above this size (half the L2) select the tile-outer
-// walk and cohort launch order for the striped layout: K and V in the forward, Q, dO and
-// the fp32 dQ accumulator in the backward.
+// walk for the striped layout: K and V in the forward, Q, dO and the fp32 dQ accumulator
+// in the backward.
 constexpr double kTileOuterBytes = 64.0 * 1024 * 1024;
-
-// Launch order of n_rank * P units (rank 0 = the heaviest unit of each shard): cohorts of
-// kCohort consecutive ranks of one shard, the shards' cohorts of equal ranks side by side,
-// heavier ranks first.  Maps the launch index idx to (rank, shard); a bijection on
-// [0, n_rank * P).
-__host__ __device__ inline void cohort_decode(int idx, int n_rank, int P, int* rank,
-                                              int* shard) {
-  const int C = n_rank < kCohort ? n_rank : kCohort;
-  const int full = n_rank / C;                 // complete cohorts per shard
-  const int head = full * C * P;
-  if (idx < head) {
-    const int grp = idx / (C * P), r = idx % (C * P);
-    *shard = r / C;
-    *rank = grp * C + r % C;
-  } else {
-    const int rem = n_rank - full * C;         // the last, partial cohort of each shard
-    const int r = idx - head;
-    *shard = r / rem;
-    *rank = full * C + r % rem;
-  }
-}
 
 // Ring schedule of one query-side unit of work: the query rows are the local 128-row
 // tiles t0 .. t0+nq-1 of shard i; ring steps k0 .. k1-1 visit KV shard j = (i - k) mod P,
@@ -123,25 +98,15 @@ __host__ __device__ inline void cohort_decode(int idx, int n_rank, int P, int* r
 //               gk = block_pos(j, u); skip gk > gq, diag gk == gq (mask b <= a);
 //   striped:    skip u > t, diag u == t (mask inside: key b visible to query a iff
 //               b < a, or b == a and j <= i), full u < t.
-// A unit may start its walk of the ring steps at k0 + rot (then k0 + rot + 1, ..., wrapping
-// at k1): the steps and their order around the ring are the same, only the first one
-// differs, so that units running side by side spread over the shards.
 // In every layout the KV tiles of shard j that query tile t0+q sees form a prefix
 // u < q_end(q, j), of which only the last can be the diagonal one (q_diag, -1 if none);
 // u_end(j) is the longest such prefix over the unit's query tiles.
 struct RingSched {
   int i, t0, nq, T, P, layout, causal, k0, k1;
-  int rot;   // the unit walks its ring steps from k0 + rot, wrapping at k1 (0 <= rot < k1 - k0)
 
   __host__ __device__ int j_of(int k) const {   // 0 <= i, k < P
     const int j = i - k;
     return j < 0 ? j + P : j;
-  }
-  // the kk-th ring step the unit takes (kk = 0 .. k1 - k0 - 1)
-  __host__ __device__ int k_at(int kk) const {
-    int r = kk + rot;
-    if (r >= k1 - k0) r -= k1 - k0;
-    return k0 + r;
   }
   __host__ __device__ int q_end(int q, int j) const {
     const int t = t0 + q;
@@ -186,15 +151,9 @@ struct RingSched {
 // positions grow with t, so the visible query tiles of a shard are a suffix t >= t_lo.
 struct BwdSched {
   int j, u, n, T, P, layout, causal;
-  int rot;   // the KV tile walks the ring steps from rot, wrapping at P (0 <= rot < P)
   __host__ __device__ int i_of(int k) const {   // 0 <= j, k < P
     const int x = j + k;
     return x >= P ? x - P : x;
-  }
-  // the kk-th ring step the KV tile takes (kk = 0 .. P - 1)
-  __host__ __device__ int k_at(int kk) const {
-    const int r = kk + rot;
-    return r >= P ? r - P : r;
   }
   __host__ __device__ long long delta(int i, int t) const {
     if (layout == RA_LAYOUT_STRIPED) return 128LL * (t - u) - (i < j ? 1 : 0);

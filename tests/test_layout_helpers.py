@@ -198,55 +198,31 @@ def test_planted_schedule_error_is_caught():
     assert oracle.ring_order(0, P) == [0, 2, 1]
 
 
-COHORT_HARNESS = r"""
+UMAX_HARNESS = r"""
 #include <cstdio>
-#include <cstdlib>
 #include "ra_internal.h"
 using namespace ra;
-int main(int argc, char** argv) {
-  const int n_rank = atoi(argv[1]), P = atoi(argv[2]);
-  for (int idx = 0; idx < n_rank * P; ++idx) {
-    int r, s;
-    cohort_decode(idx, n_rank, P, &r, &s);
-    printf("%d %d\n", r, s);
-  }
-  // u_max of a striped unit over every ring step is its longest prefix
-  const RingSched sc{1, 4, 2, 9, P, RA_LAYOUT_STRIPED, 1, 0, P};
-  printf("U %d\n", sc.u_max());
+int main() {
+  // u_max of a striped unit (query tiles 4 and 5) over every ring step: its longest prefix
+  const RingSched sc{1, 4, 2, 9, 4, RA_LAYOUT_STRIPED, 1, 0, 4};
+  // and of a contiguous unit of shard 1 (tiles 4, 5 of 9): every KV tile of shard 0
+  const RingSched sd{1, 4, 2, 9, 4, RA_LAYOUT_CONTIGUOUS, 1, 0, 4};
+  printf("U %d %d\n", sc.u_max(), sd.u_max());
   return 0;
 }
 """
 
 
-def test_cohort_launch_order(tmp_path):
-    """The launch order of the kernels' units: a bijection onto (rank, shard); cohorts of
-    kCohort consecutive ranks of one shard are consecutive; ranks never decrease from one
-    cohort round to the next (heavier units first)."""
-    src = tmp_path / "cohort.cpp"
-    src.write_text(COHORT_HARNESS)
-    exe = tmp_path / "cohort"
+def test_u_max(tmp_path):
+    """u_max, the tile-outer walk's bound: the longest visible KV-tile prefix of a unit over
+    its ring steps."""
+    src = tmp_path / "umax.cpp"
+    src.write_text(UMAX_HARNESS)
+    exe = tmp_path / "umax"
     r = subprocess.run(["g++", "-std=c++17", "-O1", "-Wall", "-I", CUDA_INC, "-I",
                         os.path.join(ROOT, "exact_blockwise_ring_gb300", "csrc"), "-I",
                         os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
-    header = open(os.path.join(ROOT, "exact_blockwise_ring_gb300", "csrc", "ra_internal.h")).read()
-    C = int(header.split("constexpr int kCohort = ")[1].split(";")[0])
-    for n_rank, P in ((1, 1), (5, 3), (16, 8), (17, 8), (40, 4), (128, 32), (256, 32), (3, 32)):
-        out = subprocess.run([str(exe), str(n_rank), str(P)], capture_output=True, text=True,
-                             timeout=60).stdout.split("\n")
-        pairs = [tuple(int(x) for x in ln.split()) for ln in out if ln and not ln.startswith("U")]
-        assert sorted(pairs) == sorted((r_, s_) for r_ in range(n_rank) for s_ in range(P))
-        c = min(C, n_rank)
-        # consecutive launch indices inside a cohort: same shard, consecutive ranks
-        pos = 0
-        while pos < len(pairs):
-            size = c if pos < (n_rank // c) * c * P else n_rank - (n_rank // c) * c
-            grp = pairs[pos:pos + size]
-            assert len({s_ for _, s_ in grp}) == 1
-            assert [r_ for r_, _ in grp] == list(range(grp[0][0], grp[0][0] + size))
-            pos += size
-        ranks = [r_ for r_, _ in pairs]
-        assert all(ranks[x] // c <= ranks[x + 1] // c for x in range(len(ranks) - 1))
-    out = subprocess.run([str(exe), "2", "4"], capture_output=True, text=True, timeout=60).stdout
-    assert "U 6" in out          # query tiles 4 and 5 of a striped shard: tiles 0..5 visible
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60).stdout
+    assert "U 6 9" in out
