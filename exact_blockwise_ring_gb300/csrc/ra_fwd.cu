@@ -305,10 +305,11 @@ __global__ void __launch_bounds__(384, 1)
 
 #define RA_ISSUE_PV(PEND, PPAR, PV, PFULL, DO_, AP_)                                          \
   do {                                                                                        \
-    if (!mbar_wait(PFULL, (PV) & 1, wc) || !mbar_wait(&v_full[PEND], PPAR, wc)) {            \
+    if (!mbar_wait(PFULL, (PV) & 1, wc) || (!v_seen && !mbar_wait(&v_full[PEND], PPAR, wc))) { \
       ok = false;                                                                             \
       break;                                                                                  \
     }                                                                                         \
+    v_seen = true;                                                                            \
     tc_fence_after();                                                                         \
     const uint64_t vd = sdesc_mnmajor(v_addr + (PEND) * C::KVB, kTile * 128);                 \
     _Pragma("unroll") for (int kk = 0; kk < kTile / 16; ++kk)                                 \
@@ -331,6 +332,8 @@ __global__ void __launch_bounds__(384, 1)
       // the PV of that tile's previous item
       auto item = [&](int u, int ue0, int ue1) -> bool {
           const int kst = n % NK, vst = n % NV;
+          // both PVs of this item use the previous item's V tile: wait for it once
+          bool v_seen = false;
           if (!mbar_wait(&k_full[kst], (n / NK) & 1, wc)) return false;
           tc_fence_after();
           const uint64_t kd = sdesc_kmajor(k_addr + kst * C::KVB);
@@ -373,6 +376,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int u = 0; u < ue && ok; ++u) ok = item(u, ue0, ue1);
         }
       }
+      bool v_seen = false;
       if (ok && pend0 >= 0) RA_ISSUE_PV(pend0, ppar0, pv0, &p_full[0], dO0, dS0);
       if (ok && pend1 >= 0) RA_ISSUE_PV(pend1, ppar1, pv1, &p_full[1], dO1, dS1);
       if (ok && n > 0) umma_commit(&v_empty[(n - 1) % NV]);

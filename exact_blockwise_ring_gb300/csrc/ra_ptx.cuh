@@ -88,9 +88,23 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
-// Wait for phase `parity` of `bar`.  Returns false if the CTA is aborting.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`.  Returns false if the CTA is aborting.  A phase that
+// has already completed is seen by the cheaper non-blocking test.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   const uint32_t a = smem_u32(bar);
+  if (mbar_test_wait(a, parity)) return true;
 #pragma unroll 1
   for (int i = 0; i < 16; ++i)
     if (mbar_try_wait(a, parity)) return true;
