@@ -24,7 +24,8 @@
 //   warp 0      producer: K, V once (TMA); per query tile Q, dO (TMA) and its 128 lse
 //               (log2 domain) and D values (bulk copies from the shard-major arrays the
 //               preprocess kernel wrote), two stages
-//   warp 1      TMEM allocator and tcgen05.mma issuer
+//   warp 1      TMEM allocator and tcgen05.mma issuer (the whole warp walks the issue
+//               loop; one elected lane issues)
 //   warps 4-11  two warpgroups, thread = key row, warpgroup g takes query columns
 //               [64g, 64g+64) in four passes of 16: P^T = exp2(S^T*c - lse2) (bf16, back
 //               into TMEM inside its own S^T columns, as the A operand of dV) and
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(640, 1)
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer ===
-    if (lane == 0) {
+    {  // the whole warp; one elected lane issues
       constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);   // S^T, dP^T
       constexpr uint32_t idKM = idesc_bf16(128, D_, false, true);     // dV, dK
       constexpr uint32_t idMM = idesc_bf16(128, BQ, true, true);      // dQ^T
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(640, 1)
       const uint64_t kMN = sdesc_mnmajor(k_addr, kTile * 128);     // K^T: M = features
       const uint64_t dsK = sdesc_kmajor(ds_addr);                  // dS^T: rows = keys
       const uint64_t dsMN = sdesc_mnmajor(ds_addr, kTile * 128);   // dS^T: N = queries
-      bool ok = mbar_wait(kv_full, 0, wc);
+      bool ok = mbar_wait_w(kv_full, 0, wc);
       tc_fence_after();
       // S^T, dP^T, dV and dK inside the allocation and disjoint
       if (!check(a.err, C::COL_S + 128 <= C::COL_DP && C::COL_DP + 128 <= C::COL_DV &&
@@ -313,50 +314,50 @@ __global__ void __launch_bounds__(640, 1)
     const uint64_t bd_ = sdesc_kmajor(BADDR);                                             \
     _Pragma("unroll") for (int kk = 0; kk < D_ / 16; ++kk) {                              \
       const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;               \
-      umma_ss(D_TM, (AK) + off, bd_ + off, idKK, kk > 0 ? 1u : 0u);                       \
+      umma_ss_w(D_TM, (AK) + off, bd_ + off, idKK, kk > 0 ? 1u : 0u);                       \
     }                                                                                     \
   } while (0)
 
       if (ok && total > 0) {
-        ok = mbar_wait(&q_full[0], 0, wc);
+        ok = mbar_wait_w(&q_full[0], 0, wc);
         tc_fence_after();
         if (ok) {
           RA_SCORES(tS, kK, q_addr);
           RA_SCORES(tDP, vK, do_addr);
-          umma_commit(s_full);
+          umma_commit_w(s_full);
         }
       }
       for (int m = 0; m < total && ok; ++m) {
         const int st = m % NSTQ, st1 = (m + 1) % NSTQ;
         const uint32_t qa = q_addr + st * C::QB, da = do_addr + st * C::QB;
-        if (!mbar_wait(ds_ready, m & 1, wc)) { ok = false; break; }
+        if (!mbar_wait_w(ds_ready, m & 1, wc)) { ok = false; break; }
         tc_fence_after();
         // dQ^T = K^T dS^T into the dP region (dP^T(m) already consumed)   (K = 128 keys);
         // first, so that the drain warps can start on it while dV and S^T(m+1) run
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tDP, kMN + ((kk * 2048) >> 4), dsMN + ((kk * 2048) >> 4), idMM,
+          umma_ss_w(tDP, kMN + ((kk * 2048) >> 4), dsMN + ((kk * 2048) >> 4), idMM,
                   kk > 0 ? 1u : 0u);
-        umma_commit(dq_full);
+        umma_commit_w(dq_full);
         // dV += P^T dO   (K = 128 query rows; P^T is read from TMEM: warpgroup g left the
         // bf16 pairs of query columns [64g, 64g+64) in TMEM columns [64g, 64g+32))
         {
           const uint64_t bd = sdesc_mnmajor(da, BQ * 128);
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)
-            umma_ts(tDV, tS + (kk / 4) * 64 + (kk % 4) * 8, bd + ((kk * 2048) >> 4), idKM,
+            umma_ts_w(tDV, tS + (kk / 4) * 64 + (kk % 4) * 8, bd + ((kk * 2048) >> 4), idKM,
                     (m > 0 || kk > 0) ? 1u : 0u);
         }
         if (m + 1 < total) {
           // S^T(m+1): the S region is free once dV(m) has read P^T(m) (in-order pipe)
-          if (!mbar_wait(&q_full[st1], ((m + 1) / NSTQ) & 1, wc)) { ok = false; break; }
+          if (!mbar_wait_w(&q_full[st1], ((m + 1) / NSTQ) & 1, wc)) { ok = false; break; }
           tc_fence_after();
           RA_SCORES(tS, kK, q_addr + st1 * C::QB);
           // dP^T(m+1) once the drain warps have read dQ^T(m) out of the dP region
-          if (!mbar_wait(dq_empty, m & 1, wc)) { ok = false; break; }
+          if (!mbar_wait_w(dq_empty, m & 1, wc)) { ok = false; break; }
           tc_fence_after();
           RA_SCORES(tDP, vK, do_addr + st1 * C::QB);
-          umma_commit(s_full);
+          umma_commit_w(s_full);
         }
         // dK += dS^T Q   (K = 128 query rows); runs under the next tile's score work
         {
@@ -364,16 +365,16 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
             const uint32_t offa = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-            umma_ss(tDK, dsK + offa, bd + ((kk * 2048) >> 4), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+            umma_ss_w(tDK, dsK + offa, bd + ((kk * 2048) >> 4), idKM, (m > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        umma_commit(ds_free);       // dS^T(m) read by dQ^T(m) and dK(m)
-        umma_commit(&q_empty[st]);  // Q(m), dO(m) read for the last time
+        umma_commit_w(ds_free);       // dS^T(m) read by dQ^T(m) and dK(m)
+        umma_commit_w(&q_empty[st]);  // Q(m), dO(m) read for the last time
       }
 #undef RA_SCORES
-      if (kChecked) misc[3] = total;             // compared at the exit
-      umma_commit(kv_final);
-      umma_commit(drain);
+      if (kChecked && lane == 0) misc[3] = total;             // compared at the exit
+      umma_commit_w(kv_final);
+      umma_commit_w(drain);
       if (!ok) mbar_wait_drain(drain, 0, a.wait_limit_ns);
     }
   } else if (warp >= 4 && warp < 12) {

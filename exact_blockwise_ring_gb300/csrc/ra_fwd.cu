@@ -19,7 +19,8 @@
 // h / G; CTAs run head after head, so the G query heads of a group, which read the same
 // K/V, are adjacent in launch order and share those tiles in L2.  Roles (384 threads):
 //   warp 0      TMA producer of Q (once) and of the K tiles (NK-stage ring)
-//   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
+//   warp 1      TMEM allocator and tcgen05.mma issuer: the whole warp walks the issue
+//               loop (descriptors stay warp-uniform) and one elected lane issues
 //   warp 2      per-shard work counter (one thread), otherwise idle
 //   warp 3      TMA producer of the V tiles (NV-stage ring)
 //   warps 4-7   softmax of query tile 0 (thread = query row = TMEM lane)
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer ===
-    if (lane == 0) {
+    {  // the whole warp; one elected lane issues
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(384, 1)
       int pend0 = -1, pend1 = -1;
       uint32_t ppar0 = 0, ppar1 = 0;
       int pv0 = 0, pv1 = 0;
-      bool ok = mbar_wait(q_full, 0, wc);
+      bool ok = mbar_wait_w(q_full, 0, wc);
       tc_fence_after();
       const uint64_t q0d = sdesc_kmajor(q_addr), q1d = sdesc_kmajor(q_addr + C::QB);
       const uint32_t dS0 = tbase + C::COL_S, dS1 = tbase + C::COL_S + 128;
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(384, 1)
 
 #define RA_ISSUE_PV(PEND, PPAR, PV, PFULL, DO_, AP_)                                          \
   do {                                                                                        \
-    if (!mbar_wait(PFULL, (PV) & 1, wc) || (!v_seen && !mbar_wait(&v_full[PEND], PPAR, wc))) { \
+    if (!mbar_wait_w(PFULL, (PV) & 1, wc) || (!v_seen && !mbar_wait_w(&v_full[PEND], PPAR, wc))) { \
       ok = false;                                                                             \
       break;                                                                                  \
     }                                                                                         \
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();                                                                         \
     const uint64_t vd = sdesc_mnmajor(v_addr + (PEND) * C::KVB, kTile * 128);                 \
     _Pragma("unroll") for (int kk = 0; kk < kTile / 16; ++kk)                                 \
-        umma_ts(DO_, (AP_) + kk * 8, vd + ((kk * 2048) >> 4), idPV,                           \
+        umma_ts_w(DO_, (AP_) + kk * 8, vd + ((kk * 2048) >> 4), idPV,                           \
                 ((PV) > 0 || kk > 0) ? 1u : 0u);                                              \
     ++(PV);                                                                                   \
     (PEND) = -1;                                                                              \
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(384, 1)
   do {                                                                                        \
     _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                   \
       const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;                   \
-      umma_ss(DS_, (QD) + off, kd + off, idS, kk > 0 ? 1u : 0u);                              \
+      umma_ss_w(DS_, (QD) + off, kd + off, idS, kk > 0 ? 1u : 0u);                              \
     }                                                                                         \
   } while (0)
 
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(384, 1)
           const int kst = n % NK, vst = n % NV;
           // both PVs of this item use the previous item's V tile: wait for it once
           bool v_seen = false;
-          if (!mbar_wait(&k_full[kst], (n / NK) & 1, wc)) return false;
+          if (!mbar_wait_w(&k_full[kst], (n / NK) & 1, wc)) return false;
           tc_fence_after();
           const uint64_t kd = sdesc_kmajor(k_addr + kst * C::KVB);
           // query tile 0
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(384, 1)
           if (u < ue0) {
             RA_ISSUE_S(q0d, dS0);
             ++n_s0;
-            umma_commit(&s_full[0]);
+            umma_commit_w(&s_full[0]);
             pend0 = vst;
             ppar0 = (n / NV) & 1;
           }
@@ -354,12 +355,12 @@ __global__ void __launch_bounds__(384, 1)
           if (u < ue1) {
             RA_ISSUE_S(q1d, dS1);
             ++n_s1;
-            umma_commit(&s_full[1]);
+            umma_commit_w(&s_full[1]);
             pend1 = vst;
             ppar1 = (n / NV) & 1;
           }
-          umma_commit(&k_empty[kst]);                       // both S MMAs of item n issued
-          if (n > 0) umma_commit(&v_empty[(n - 1) % NV]);    // every PV of item n-1 issued
+          umma_commit_w(&k_empty[kst]);                       // both S MMAs of item n issued
+          if (n > 0) umma_commit_w(&v_empty[(n - 1) % NV]);    // every PV of item n-1 issued
           ++n;
           return true;
       };
@@ -379,17 +380,17 @@ __global__ void __launch_bounds__(384, 1)
       bool v_seen = false;
       if (ok && pend0 >= 0) RA_ISSUE_PV(pend0, ppar0, pv0, &p_full[0], dO0, dS0);
       if (ok && pend1 >= 0) RA_ISSUE_PV(pend1, ppar1, pv1, &p_full[1], dO1, dS1);
-      if (ok && n > 0) umma_commit(&v_empty[(n - 1) % NV]);
+      if (ok && n > 0) umma_commit_w(&v_empty[(n - 1) % NV]);
 #undef RA_ISSUE_PV
 #undef RA_ISSUE_S
-      if (kChecked) {                           // compared at the exit
+      if (kChecked && lane == 0) {              // compared at the exit
         misc[4] = n;
         misc[5] = n_s0;
         misc[6] = n_s1;
       }
-      umma_commit(&o_final[0]);
-      umma_commit(&o_final[1]);
-      umma_commit(drain);
+      umma_commit_w(&o_final[0]);
+      umma_commit_w(&o_final[1]);
+      umma_commit_w(drain);
       if (!ok) mbar_wait_drain(drain, 0, a.wait_limit_ns);
     }
   } else if (warp == 2) {
