@@ -22,7 +22,8 @@
 //   warp 1      TMEM allocator and tcgen05.mma issuer: the whole warp walks the issue
 //               loop (descriptors stay warp-uniform) and one elected lane issues
 //   warp 2      per-shard work counter (one thread), otherwise idle
-//   warp 3      TMA producer of the V tiles (NV-stage ring)
+//   warp 3      TMA producer of the V tiles (NV-stage ring); both producer warps walk
+//               their loops as whole warps, one elected lane issuing the copies
 //   warps 4-7   softmax of query tile 0 (thread = query row = TMEM lane)
 //   warps 8-11  softmax of query tile 1
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0 || warp == 3) {
     // ================================================================ producers ====
     // warp 0: Q once, then K tiles; warp 3: V tiles.  Both walk the same item sequence.
-    if (lane == 0) {
+    {  // the whole warp; one elected lane issues
       const bool is_k = warp == 0;
       const int NS = is_k ? NK : NV;
       uint64_t* full = is_k ? k_full : v_full;
@@ -245,24 +246,24 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(tm);
       if (is_k) {
         tma_prefetch_desc(&tmQ);
-        mbar_expect_tx(q_full, nvalid * C::QB);
+        mbar_expect_tx_w(q_full, nvalid * C::QB);
         for (int q = 0; q < nvalid; ++q)
           for (int cb = 0; cb < C::NCB; ++cb)
             if (check(a.err, rows_box_ok(cb * 64, h, i, (2 * s + q) * kTile, b, a.n, a.P, a.H,
                                          a.B, D), kChkTma))
-              load_rows(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h,
+              load_rows<true>(sQ + q * C::QB + cb * kTile * 128, &tmQ, q_full, a.layout, cb * 64, h,
                         i, (2 * s + q) * kTile, b, a.n, a.P);
       }
       int n = 0;
       bool ok = true;
       auto item = [&](int u, int j) {
         const int st = n % NS;
-        if (n >= NS && !mbar_wait(&empty[st], ((n / NS) - 1) & 1, wc)) return false;
-        mbar_expect_tx(&full[st], C::KVB);
+        if (n >= NS && !mbar_wait_w(&empty[st], ((n / NS) - 1) & 1, wc)) return false;
+        mbar_expect_tx_w(&full[st], C::KVB);
         for (int cb = 0; cb < C::NCB; ++cb)
           if (check(a.err, rows_box_ok(cb * 64, hkv, j, u * kTile, b, a.n, a.P, a.H / a.G, a.B,
                                        D) && st < NS, kChkTma))
-            load_rows(ring + st * C::KVB + cb * kTile * 128, tm, &full[st], a.layout, cb * 64,
+            load_rows<true>(ring + st * C::KVB + cb * kTile * 128, tm, &full[st], a.layout, cb * 64,
                       hkv, j, u * kTile, b, a.n, a.P);
         ++n;
         return true;
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int u = 0; u < ue && ok; ++u) ok = item(u, j);
         }
       }
-      if (kChecked) misc[is_k ? 2 : 3] = n;     // items loaded, compared at the exit
+      if (kChecked && lane == 0) misc[is_k ? 2 : 3] = n;     // items loaded, compared at the exit
       // let every copy this thread issued land before the CTA can exit
       if (is_k) mbar_wait_drain(q_full, 0, a.wait_limit_ns);
       for (int m = (n > NS ? n - NS : 0); m < n; ++m)

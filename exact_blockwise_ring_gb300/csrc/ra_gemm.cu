@@ -14,6 +14,8 @@
 //   warp 1      TMEM owner (512 columns: two 256-column accumulators) and tcgen05.mma
 //               issuer: M = 128, N = 256, K = 16 per instruction, both operands K-major
 //               from shared memory; tile i accumulates in buffer i mod 2
+//   (warps 0 and 1 each walk their loop as a whole warp, with warp-uniform descriptors
+//   and coordinates; one elected lane issues every copy, MMA and commit)
 //   warps 2-5   epilogue, thread = output row = TMEM lane: 32 columns at a time out of
 //               TMEM, bias / GELU / residual in registers, 16-byte stores; it releases an
 //               accumulator as soon as it has read it, so a tile's epilogue runs under
@@ -52,6 +54,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_w(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int c0, int c1) {
+  asm volatile(
+      RA_ELECTED("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4}], [%2];") ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
@@ -147,7 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ================================================================ producer =====
-    if (lane == 0) {
+    {  // the whole warp; one elected lane issues
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       int it = 0;                               // K steps issued, over all tiles
@@ -157,11 +168,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tile_of(pid, mt, nt, tm, tn);
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages;
-          if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, wc)) {
+          if (it >= kStages && !mbar_wait_w(&empty[s], ((it / kStages) - 1) & 1, wc)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&full[s], kAB + kBB);
+          mbar_expect_tx_w(&full[s], kAB + kBB);
           // the tile's boxes inside A [M, K] and B [N, K]
           if (!check(g.err, tm >= 0 && (tm + 1) * GM <= g.M && tn >= 0 && (tn + 1) * GN <= g.N &&
                                 (kb + 1) * GK <= g.K && s < kStages, kChkTma))
@@ -170,27 +181,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (A_MN) {
 #pragma unroll
             for (int b4 = 0; b4 < GM / 64; ++b4)
-              tma_load_2d(sA + s * kAB + b4 * 8192, &tmA, &full[s], tm * GM + 64 * b4, kb * GK);
+              tma_load_2d_w(sA + s * kAB + b4 * 8192, &tmA, &full[s], tm * GM + 64 * b4, kb * GK);
           } else {
-            tma_load_2d(sA + s * kAB, &tmA, &full[s], kb * GK, tm * GM);
+            tma_load_2d_w(sA + s * kAB, &tmA, &full[s], kb * GK, tm * GM);
           }
           if (B_MN) {
 #pragma unroll
             for (int b4 = 0; b4 < GN / 64; ++b4)
-              tma_load_2d(sB + s * kBB + b4 * 8192, &tmB, &full[s], tn * GN + 64 * b4, kb * GK);
+              tma_load_2d_w(sB + s * kBB + b4 * 8192, &tmB, &full[s], tn * GN + 64 * b4, kb * GK);
           } else {
-            tma_load_2d(sB + s * kBB, &tmB, &full[s], kb * GK, tn * GN);
+            tma_load_2d_w(sB + s * kBB, &tmB, &full[s], kb * GK, tn * GN);
           }
         }
       }
-      if (kChecked) misc[2] = it;                // K steps loaded, compared at the exit
+      if (kChecked && lane == 0) misc[2] = it;                // K steps loaded, compared at the exit
       // let every copy this thread issued land before the CTA can exit
       for (int r = (it > kStages ? it - kStages : 0); r < it; ++r)
         wait_drain(&full[r % kStages], (r / kStages) & 1, g.wait_limit_ns);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer ===
-    if (lane == 0) {
+    {  // the whole warp; one elected lane issues
       constexpr uint32_t idesc = idesc_bf16(GM, GN, A_MN != 0, B_MN != 0);
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
       int it = 0, lt = 0;
@@ -200,11 +211,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t tacc = tbase + buf * GN;
         if (!check(g.err, buf * GN + GN <= 512, kChkTmem)) { ok = false; break; }
         // the epilogue has read this accumulator's previous tile out of TMEM
-        if (lt >= 2 && !mbar_wait(&acc_empty[buf], ((lt >> 1) - 1) & 1, wc)) { ok = false; break; }
+        if (lt >= 2 && !mbar_wait_w(&acc_empty[buf], ((lt >> 1) - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages;
-          if (!mbar_wait(&full[s], (it / kStages) & 1, wc)) { ok = false; break; }
+          if (!mbar_wait_w(&full[s], (it / kStages) & 1, wc)) { ok = false; break; }
           tc_fence_after();
           // K-major: +32 bytes per K step of 16; MN-major: +16 rows of 128 bytes, with the
           // 64-wide M (N) blocks 8 KB apart
@@ -212,14 +223,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t bd = B_MN ? sdesc_mnmajor(b0 + s * kBB, 8192) : sdesc_kmajor(b0 + s * kBB);
 #pragma unroll
           for (int kk = 0; kk < GK / 16; ++kk)
-            umma_ss(tacc, ad + (A_MN ? 128 : 2) * kk, bd + (B_MN ? 128 : 2) * kk, idesc,
+            umma_ss_w(tacc, ad + (A_MN ? 128 : 2) * kk, bd + (B_MN ? 128 : 2) * kk, idesc,
                     (kb > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&empty[s]);
+          umma_commit_w(&empty[s]);
         }
-        if (ok) umma_commit(&acc_full[buf]);
+        if (ok) umma_commit_w(&acc_full[buf]);
       }
-      if (kChecked) misc[3] = it;                // compared at the exit
-      umma_commit(drain);
+      if (kChecked && lane == 0) misc[3] = it;                // compared at the exit
+      umma_commit_w(drain);
       wait_drain(drain, 0, g.wait_limit_ns);     // every MMA done before TMEM is released
     }
   } else {

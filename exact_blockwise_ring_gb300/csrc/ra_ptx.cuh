@@ -132,6 +132,26 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Warp-wide form of a TMA copy or a producer arrive: every lane of a converged warp
+// executes it with the same operands; one elected lane issues it.
+#define RA_ELECTED(INSTR) "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t@e " INSTR "\n\t}"
+
+__device__ __forceinline__ void tma_load_5d_w(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      RA_ELECTED("cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];") ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx_w(uint64_t* bar, uint32_t bytes) {
+  asm volatile(RA_ELECTED("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;")
+               ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05 ----------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

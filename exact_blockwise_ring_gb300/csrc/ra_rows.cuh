@@ -13,18 +13,23 @@ namespace ra {
 //   zigzag     dims (D, H, c, 2P, B):  coordinates (d0, h, local mod c, chunk, b), with
 //              chunk = shard for local < c and 2P-1-shard otherwise; c = n/2 is a multiple
 //              of 128, so a box never straddles the two chunks.
+// W: the whole converged warp calls it and one elected lane issues the copy.
+template <bool W = false>
 __device__ __forceinline__ void load_rows(void* dst, const CUtensorMap* m, uint64_t* bar,
                                           int layout, int d0, int h, int shard, int local0,
                                           int b, int n, int P) {
-  if (layout == RA_LAYOUT_STRIPED) {
-    tma_load_5d(dst, m, bar, d0, h, shard, local0, b);
-  } else if (layout == RA_LAYOUT_ZIGZAG) {
+  int c2 = shard, c3 = local0;                  // striped: (shard, local)
+  if (layout == RA_LAYOUT_ZIGZAG) {
     const int c = n >> 1;
     const bool lo = local0 < c;
-    tma_load_5d(dst, m, bar, d0, h, lo ? local0 : local0 - c, lo ? shard : 2 * P - 1 - shard, b);
-  } else {
-    tma_load_5d(dst, m, bar, d0, h, local0, shard, b);
+    c2 = lo ? local0 : local0 - c;
+    c3 = lo ? shard : 2 * P - 1 - shard;
+  } else if (layout != RA_LAYOUT_STRIPED) {     // contiguous: (local, shard)
+    c2 = local0;
+    c3 = shard;
   }
+  if (W) tma_load_5d_w(dst, m, bar, d0, h, c2, c3, b);
+  else tma_load_5d(dst, m, bar, d0, h, c2, c3, b);
 }
 
 // The box load_rows reads (64 features from d0, 128 local rows from local0, one head,
