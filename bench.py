@@ -478,10 +478,11 @@ def run_ours(args, w, rank, world, local):
             e2e_step(sidx)
         torch.cuda.synchronize()
         # three timed windows of Ke steps each (Ke = K, or fewer when K steps take over
-        # 10 s: seconds-long steps hide their copies anyway); the line reports the median
-        # window and lists all three (on a virtualised host a single host-memory copy can
-        # stall for ~100 ms, which one window cannot absorb)
-        Ke = K if ms_per_step * K <= 10000.0 else max(1, int(10000.0 // ms_per_step))
+        # 10 s, but two at least when K allows, so that a window holds a step whose copies
+        # run under its neighbour's compute; about 15 s of steps at most); the line reports
+        # the median window and lists all three (on a virtualised host a single host-memory
+        # copy can stall for ~100 ms, which one window cannot absorb)
+        Ke = K if ms_per_step * K <= 10000.0 else max(min(K, 2), int(15000.0 // ms_per_step))
         windows = []
         for _ in range(3):
             dist_barrier(world)
