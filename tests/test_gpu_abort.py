@@ -22,6 +22,8 @@ TIMEOUT_WORD = 0x7          # what a wait that gave up writes
 
 
 def _plant(ws):
+    # on the buffer the next calls will use: a workspace grows (into a fresh zeroed
+    # buffer) on the first call that needs more, so the tests size it with a clean call
     ws.buf[:4].view(torch.int32).fill_(TIMEOUT_WORD)
 
 
@@ -30,6 +32,9 @@ def test_attention_kernels_leave_at_once_after_a_recorded_failure(layout):
     q, k, v, do = make_inputs(1, 2048, 2, 128, seed=77)
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
     ws = era.Workspace(torch.device("cuda:0"))
+    out, lse = era.ra_fwd(qd, kd, vd, 4, 128, layout, True, workspace=ws)
+    era.ra_bwd(qd, kd, vd, out, lse, dod, 4, 128, layout, True, workspace=ws)
+    ws.check()
 
     _plant(ws)
     out, lse = era.ra_fwd(qd, kd, vd, 4, 128, layout, True, workspace=ws)
@@ -54,6 +59,8 @@ def test_split_forward_and_merge_after_a_recorded_failure():
     q, k, v, _ = make_inputs(1, 1024, 2, 128, seed=78)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     ws = era.Workspace(torch.device("cuda:0"))
+    era.ra_fwd(qd, kd, vd, 4, 128, "striped", True, n_split=0, workspace=ws)
+    ws.check()
     _plant(ws)
     era.ra_fwd(qd, kd, vd, 4, 128, "striped", True, n_split=0, workspace=ws)
     with pytest.raises(era.RaError, match="RA_ERR_DEVICE_TIMEOUT"):
@@ -72,6 +79,8 @@ def test_layer_gemm_after_a_recorded_failure():
     w = (torch.randn(512, 256, generator=g) / 16).to(torch.bfloat16).cuda()
     bias = torch.randn(512, generator=g).cuda()
     ws = era.Workspace(torch.device("cuda:0"))
+    era.ra_linear(x, w, bias, "bias", workspace=ws)
+    ws.check()
     _plant(ws)
     era.ra_linear(x, w, bias, "bias", workspace=ws)
     with pytest.raises(era.RaError, match="RA_ERR_DEVICE_TIMEOUT"):
