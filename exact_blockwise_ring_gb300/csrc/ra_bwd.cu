@@ -330,6 +330,9 @@ __global__ void __launch_bounds__(640, 1)
       for (int m = 0; m < total && ok; ++m) {
         const int st = m % NSTQ, st1 = (m + 1) % NSTQ;
         const uint32_t qa = q_addr + st * C::QB, da = do_addr + st * C::QB;
+        // the next Q/dO stage (loaded long before) is tested while the score warps still
+        // work, inside the wait below rather than between products
+        if (m + 1 < total && !mbar_wait_w(&q_full[st1], ((m + 1) / NSTQ) & 1, wc)) { ok = false; break; }
         if (!mbar_wait_w(ds_ready, m & 1, wc)) { ok = false; break; }
         tc_fence_after();
         // dQ^T = K^T dS^T into the dP region (dP^T(m) already consumed)   (K = 128 keys);
@@ -350,8 +353,6 @@ __global__ void __launch_bounds__(640, 1)
         }
         if (m + 1 < total) {
           // S^T(m+1): the S region is free once dV(m) has read P^T(m) (in-order pipe)
-          if (!mbar_wait_w(&q_full[st1], ((m + 1) / NSTQ) & 1, wc)) { ok = false; break; }
-          tc_fence_after();
           RA_SCORES(tS, kK, q_addr + st1 * C::QB);
           // dP^T(m+1) once the drain warps have read dQ^T(m) out of the dP region
           if (!mbar_wait_w(dq_empty, m & 1, wc)) { ok = false; break; }

@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(384, 1)
 
 #define RA_ISSUE_PV(PEND, PPAR, PV, PFULL, DO_, AP_)                                          \
   do {                                                                                        \
-    if (!mbar_wait_w(PFULL, (PV) & 1, wc) || (!v_seen && !mbar_wait_w(&v_full[PEND], PPAR, wc))) { \
+    if ((!v_seen && !mbar_wait_w(&v_full[PEND], PPAR, wc)) || !mbar_wait_w(PFULL, (PV) & 1, wc)) { \
       ok = false;                                                                             \
       break;                                                                                  \
     }                                                                                         \
